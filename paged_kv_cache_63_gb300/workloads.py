@@ -1,0 +1,187 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic, so both the CUDA path and the CPU oracle can consume its
+output without sharing any of the method's code.
+
+Layouts follow "[TIL] Optimizing paged attention" (retepy.com), section
+"Data Layout" and the block-table sketch in section "Baseline":
+
+* ``query``           fp16 ``[batch][query_heads][head_dim]`` (one token per sequence)
+* ``key_cache``       fp16 ``[num_physical_pages][page_size][kv_heads][head_dim]``
+* ``value_cache``     same layout as ``key_cache``
+* ``block_tables``    int32 ``[batch][max_pages_per_sequence]``; entries past
+  ``ceil(context_length / page_size)`` are placeholders, filled with -1 here
+* ``context_lengths`` int32 ``[batch]``
+
+Random draws (numpy PCG64 via ``default_rng``), in this order: context lengths
+(if random), the physical-page permutation, then q, the K pool and the V pool as
+float32 standard normals (K multiplied by ``k_scale`` first), each rounded to
+fp16 with round-to-nearest-even. Large pools are drawn in fixed-size chunks from
+the same generator, which yields the same stream as one big draw.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional
+
+import numpy as np
+
+# Chunk of float32 normals drawn at a time when filling a large pool.
+_CHUNK = 1 << 24
+
+
+@dataclasses.dataclass(frozen=True)
+class Spec:
+    """Shape and distribution recipe of one workload."""
+
+    name: str
+    batch: int
+    query_heads: int
+    kv_heads: int
+    head_dim: int
+    page_size: int
+    max_pages_per_sequence: int
+    seed: int
+    # context-length recipe: ("fixed", [lens]) | ("uniform", lo, hi) |
+    # ("lognormal", mu, sigma, lo, hi, n_ones)
+    ctx: tuple
+    # how physical pages are assigned: "tiny16" (16-page pool, seeded
+    # permutation) or "shuffled" (pool sized to the total need, permuted)
+    pages: str = "shuffled"
+    k_scale: float = 1.0
+
+
+# The five workloads of this library's test and benchmark plan.
+SPECS: Dict[str, Spec] = {
+    "tiny": Spec("tiny", batch=2, query_heads=4, kv_heads=2, head_dim=64, page_size=16,
+                 max_pages_per_sequence=8, seed=0, ctx=("fixed", [37, 100]), pages="tiny16"),
+    "gqa4_mid": Spec("gqa4_mid", batch=32, query_heads=32, kv_heads=8, head_dim=128,
+                     page_size=16, max_pages_per_sequence=256, seed=1,
+                     ctx=("uniform", 512, 4096)),
+    "mha": Spec("mha", batch=64, query_heads=32, kv_heads=32, head_dim=128, page_size=16,
+                max_pages_per_sequence=128, seed=2, ctx=("fixed", [2048] * 64)),
+    "long_gqa6": Spec("long_gqa6", batch=4, query_heads=24, kv_heads=4, head_dim=256,
+                      page_size=64, max_pages_per_sequence=1563, seed=3,
+                      ctx=("fixed", [100000] * 4), k_scale=0.5),
+    "ragged": Spec("ragged", batch=256, query_heads=64, kv_heads=8, head_dim=128,
+                   page_size=32, max_pages_per_sequence=1024, seed=4,
+                   ctx=("lognormal", 7.0, 1.2, 1, 32768, 4)),
+}
+
+
+@dataclasses.dataclass
+class Workload:
+    """One decode step's inputs (host numpy arrays)."""
+
+    spec: Spec
+    batch: int
+    query_heads: int
+    kv_heads: int
+    head_dim: int
+    page_size: int
+    max_pages_per_sequence: int
+    num_physical_pages: int
+    scale: float
+    query: np.ndarray
+    key_cache: np.ndarray
+    value_cache: np.ndarray
+    block_tables: np.ndarray
+    context_lengths: np.ndarray
+
+    @property
+    def name(self) -> str:
+        return self.spec.name
+
+    def dims(self) -> dict:
+        return dict(batch=self.batch, query_heads=self.query_heads, kv_heads=self.kv_heads,
+                    head_dim=self.head_dim, page_size=self.page_size,
+                    max_pages_per_sequence=self.max_pages_per_sequence,
+                    num_physical_pages=self.num_physical_pages)
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V that one decode step must read (each once)."""
+        return int(self.context_lengths.astype(np.int64).clip(min=0).sum()) * \
+            self.kv_heads * self.head_dim * 2 * 2
+
+
+def _draw_fp16(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
+    out = np.empty(shape, dtype=np.float16)
+    flat = out.reshape(-1)
+    n = flat.size
+    for lo in range(0, n, _CHUNK):
+        hi = min(n, lo + _CHUNK)
+        x = rng.standard_normal(hi - lo, dtype=np.float32)
+        if scale != 1.0:
+            x *= np.float32(scale)
+        flat[lo:hi] = x.astype(np.float16)
+    return out
+
+
+def _context_lengths(spec: Spec, rng: np.random.Generator, batch: int) -> np.ndarray:
+    kind = spec.ctx[0]
+    if kind == "fixed":
+        lens = list(spec.ctx[1])
+        if len(lens) != batch:
+            lens = [lens[i % len(lens)] for i in range(batch)]
+        return np.asarray(lens, dtype=np.int32)
+    if kind == "uniform":
+        lo, hi = spec.ctx[1], spec.ctx[2]
+        return rng.integers(lo, hi + 1, size=batch).astype(np.int32)
+    if kind == "lognormal":
+        mu, sigma, lo, hi, n_ones = spec.ctx[1:]
+        x = np.clip(np.rint(rng.lognormal(mu, sigma, size=batch)), lo, hi).astype(np.int32)
+        ones = rng.choice(batch, size=min(n_ones, batch), replace=False)
+        x[ones] = 1
+        return x
+    raise ValueError(f"unknown context recipe {kind!r}")
+
+
+def make_workload(name: str, seed: Optional[int] = None, *, batch: Optional[int] = None,
+                  context_lengths=None, max_pages_per_sequence: Optional[int] = None,
+                  spare_pages: int = 0, **override) -> Workload:
+    """Build one seeded workload.
+
+    ``batch``, ``context_lengths`` and ``max_pages_per_sequence`` shrink or reshape a
+    workload for tests that must finish on the oracle in seconds; ``spare_pages``
+    adds unreferenced physical pages to the pool; other keyword arguments override
+    fields of the spec (e.g. ``page_size=64``).
+    """
+    spec = SPECS[name]
+    if override:
+        spec = dataclasses.replace(spec, **override)
+    seed = spec.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    b = spec.batch if batch is None else batch
+    hd, ps, kvh, qh = spec.head_dim, spec.page_size, spec.kv_heads, spec.query_heads
+
+    if context_lengths is not None:
+        ctx = np.asarray(context_lengths, dtype=np.int32).reshape(-1)
+        b = ctx.size
+    else:
+        ctx = _context_lengths(spec, rng, b)
+    need = [max(0, -(-int(c) // ps)) for c in ctx]
+    maxp = spec.max_pages_per_sequence if max_pages_per_sequence is None else max_pages_per_sequence
+    maxp = max(maxp, max(need) if need else 1, 1)
+
+    if spec.pages == "tiny16" and context_lengths is None and batch is None:
+        pool = 16
+    else:
+        pool = sum(need) + spare_pages
+    pool = max(pool, 1)
+    perm = rng.permutation(pool).astype(np.int32)
+    bt = np.full((b, maxp), -1, dtype=np.int32)
+    off = 0
+    for i, n in enumerate(need):
+        bt[i, :n] = perm[off:off + n]
+        off += n
+
+    q = _draw_fp16(rng, (b, qh, hd))
+    k = _draw_fp16(rng, (pool, ps, kvh, hd), spec.k_scale)
+    v = _draw_fp16(rng, (pool, ps, kvh, hd))
+    return Workload(spec=spec, batch=b, query_heads=qh, kv_heads=kvh, head_dim=hd,
+                    page_size=ps, max_pages_per_sequence=maxp, num_physical_pages=pool,
+                    scale=1.0 / math.sqrt(hd), query=q, key_cache=k, value_cache=v,
+                    block_tables=bt, context_lengths=ctx)
