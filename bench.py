@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of one paged decode step (libpagedattn.pa_decode) on GB300.
+
+A bench step is one pa_decode call over the whole batch of the named workload (inputs
+resident in HBM), with L2 flushed (a 256 MiB write) before every step, outside the timed
+interval. Prints one JSON line (rank 0): KV-cache read GB/s, microseconds per call, the
+roofline of the decode kernel against the measured HBM copy bandwidth, SM clocks sampled
+during the timed region, an end-to-end figure through the C ABI with the per-step inputs
+copied from pinned host memory, and the CPU oracle timed on the host cores.
+
+``--impl reference`` times the CPU oracle itself (there is no runnable reference library
+for this method) on the same workload and metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and μs per call"
+DEFAULT_WORKLOAD = "gqa4_mid"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["device_common.cuh", "decode_kernel.cuh", "decode_launch.cuh", "internal.h",
+                  "api.cpp", "launch.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the short per-workload summary of the other workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work for the oracle baseline sample")
+    ap.add_argument("--math", default="auto")
+    ap.add_argument("--schedule", default="auto")
+    ap.add_argument("--combine", default="fused")
+    ap.add_argument("--workers", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--warps", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_63_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on the current
+    kernel sources (profiles/traffic.json maps workload -> {kernel_hash, dram_bytes})."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def algorithmic_bytes(w) -> dict:
+    ctx = w.context_lengths.astype(np.int64).clip(min=0)
+    kv = int(ctx.sum()) * w.kv_heads * w.head_dim * 2 * 2
+    q = w.batch * w.query_heads * w.head_dim * 2
+    out = w.batch * w.query_heads * w.head_dim * 4
+    bt = int((-(-ctx // w.page_size)).sum()) * 4 + w.batch * 4
+    return dict(kv=kv, total=kv + q + out + bt, h2d=q + w.block_tables.nbytes + ctx.size * 4,
+                d2h=out)
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, busy_from: float = 0.0) -> dict:
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 8:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        load = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sm)}
+
+
+def to_device(w, torch):
+    return dict(q=torch.from_numpy(w.query).cuda(), k=torch.from_numpy(w.key_cache).cuda(),
+                v=torch.from_numpy(w.value_cache).cuda(), bt=torch.from_numpy(w.block_tables).cuda(),
+                ctx=torch.from_numpy(w.context_lengths).cuda(),
+                out=torch.empty((w.batch, w.query_heads, w.head_dim), dtype=torch.float32,
+                                device="cuda"))
+
+
+def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=False):
+    """Per-step CUDA-event times (ms) of pa_decode_ex, L2 flushed before each step."""
+    prob = lib.problem_of(w)
+    n = lib.pa_workspace_size(prob, opts)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+    lib.pa_workspace_init(ws, n)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    host = None
+    if e2e:
+        host = dict(q=torch.from_numpy(w.query).pin_memory(),
+                    bt=torch.from_numpy(w.block_tables).pin_memory(),
+                    ctx=torch.from_numpy(w.context_lengths).pin_memory(),
+                    out=torch.empty(d["out"].shape, dtype=torch.float32).pin_memory())
+
+    def step():
+        if e2e:
+            d["q"].copy_(host["q"], non_blocking=True)
+            d["bt"].copy_(host["bt"], non_blocking=True)
+            d["ctx"].copy_(host["ctx"], non_blocking=True)
+        lib.pa_decode_ex(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"], opts,
+                         ws if n else None, n, stream.cuda_stream)
+        if e2e:
+            host["out"].copy_(d["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    world, _, _ = dist_env()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(sampler_dev) if sampler_dev is not None else None
+    if sampler:
+        sampler.__enter__()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    if sampler:
+        sampler.__exit__(None, None, None)
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks = sampler.summary() if sampler else None
+    return ms, wall, clocks
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    """The fp64 oracle on the host cores over a bounded sample of the same workload: all
+    query heads of a subset of sequences (calibrated to about `seconds` of work)."""
+    import oracle
+
+    oracle.build()
+    g = w.query_heads
+    order = np.argsort(w.context_lengths)[::-1]
+    b0 = int(order[len(order) // 2])  # a median-length sequence to calibrate on
+    t0 = time.perf_counter()
+    oracle.decode(w, rows=np.arange(b0 * g, (b0 + 1) * g))
+    t_one = max(time.perf_counter() - t0, 1e-4)
+    n_seq = int(max(1, min(w.batch, seconds / t_one)))
+    rng = np.random.default_rng(7)
+    seqs = np.sort(rng.choice(w.batch, size=n_seq, replace=False))
+    rows = np.concatenate([np.arange(b * g, (b + 1) * g) for b in seqs])
+    t0 = time.perf_counter()
+    oracle.decode(w, rows=rows)
+    dt = time.perf_counter() - t0
+    kv = int(w.context_lengths[seqs].astype(np.int64).sum()) * w.kv_heads * w.head_dim * 4
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{n_seq} of {w.batch} sequences (all {g} query heads each), "
+                      f"{kv / 1e6:.1f} MB of K/V, {dt:.2f} s"}
+
+
+def config_of(w, plan, extra=None):
+    c = {"workload": w.name, "batch": w.batch, "query_heads": w.query_heads,
+         "kv_heads": w.kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+         "max_pages_per_sequence": w.max_pages_per_sequence,
+         "context_tokens": int(w.context_lengths.sum()),
+         "l2": "flushed before every step (256 MiB write, outside the timed interval)",
+         "schedule": ["auto", "single", "balanced"][plan["schedule"]],
+         "math": ["auto", "simt", "mma"][plan["math"]],
+         "workers": plan["workers"], "stages": plan["stages"],
+         "warps_per_cta": plan["warps_per_cta"], "parallelism": "replicas"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_ours(args):
+    import torch
+
+    from paged_kv_cache_63_gb300 import lib
+    from paged_kv_cache_63_gb300.workloads import make_workload
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    lib.load()
+    opts = lib.options(schedule=args.schedule, math=args.math, combine=args.combine,
+                       workers=args.workers, stages=args.stages, warps_per_cta=args.warps)
+    sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    seed = None if rank == 0 else 1000 + rank  # each rank decodes its own batch
+    w = make_workload(args.workload, seed=seed)
+    plan = lib.pa_plan(lib.problem_of(w), opts, sm_count)
+    d = to_device(w, torch)
+    nbytes = algorithmic_bytes(w)
+    dev_index = torch.cuda.current_device()
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    smi_index = int(phys[dev_index]) if phys and phys[0].strip().isdigit() else dev_index
+    ms, wall, clocks = time_decode(w, d, opts, args.steps, args.warmup, torch, lib,
+                                   sampler_dev=smi_index if rank == 0 else None)
+    assert lib.pa_get_device_error() == 0
+    t = torch.tensor([sum(ms) / len(ms)], dtype=torch.float64, device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_step = float(t.item())
+    e2e_ms, _, _ = time_decode(w, d, opts, max(10, args.steps // 4), args.warmup, torch, lib,
+                               e2e=True)
+    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    if rank != 0:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_peak()
+    achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9
+    kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
+    launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 1) else 1
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC,
+        "value": round(kv_gbs * world, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2),
+        "pct_of_hbm_peak": round(100 * kv_gbs / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "accumulate": "f32",
+        "data": "synthetic (seeded numpy draws of the workload's shapes and length mix)",
+        "config": config_of(w, plan, {"kv_bytes": nbytes["kv"]}),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": nbytes["total"],
+                     "kernel": "pa::decode_kernel"},
+        "clocks": clocks,
+        "e2e": {"value": round(nbytes["kv"] / (e2e_step * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+                "us_per_call": round(e2e_step * 1e3, 2),
+                "h2d_bytes_per_step": nbytes["h2d"], "d2h_bytes_per_step": nbytes["d2h"],
+                "note": "q, block tables and context lengths copied from pinned host memory and "
+                        "the output copied back every step; the K/V cache is resident state"},
+        "gpu_launches": args.steps * launches_per_call,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    del d
+    torch.cuda.empty_cache()
+    if not args.no_others:
+        others = {}
+        for name in ("mha", "long_gqa6", "ragged"):
+            if name == w.name:
+                continue
+            wo = make_workload(name)
+            do = to_device(wo, torch)
+            po = lib.pa_plan(lib.problem_of(wo), opts, sm_count)
+            mso, _, _ = time_decode(wo, do, opts, 200, 10, torch, lib)
+            m = sum(mso) / len(mso)
+            nb = algorithmic_bytes(wo)
+            others[name] = {"us_per_call": round(m * 1e3, 2),
+                            "kv_gbs": round(nb["kv"] / (m * 1e-3) / 1e9, 1),
+                            "frac_of_peak": round(nb["total"] / (m * 1e-3) / 1e9 / peak, 4),
+                            "schedule": ["auto", "single", "balanced"][po["schedule"]],
+                            "workers": po["workers"]}
+            del do
+            torch.cuda.empty_cache()
+        line["other_workloads"] = others
+    line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step decodes a bounded sample of the
+    workload (all heads of a few sequences) on the host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_cache_63_gb300.workloads import make_workload
+
+    oracle.build()
+    w = make_workload(args.workload)
+    g = w.query_heads
+    budget = 120.0 / max(1, args.steps + args.warmup)  # seconds of CPU work per step
+    b0 = int(np.argsort(w.context_lengths)[len(w.context_lengths) // 2])
+    t0 = time.perf_counter()
+    oracle.decode(w, rows=np.arange(b0 * g, (b0 + 1) * g))
+    t_seq = max(time.perf_counter() - t0, 1e-4)
+    if budget >= t_seq:
+        rows = np.arange(b0 * g, (b0 + 1) * g)
+        kv = int(w.context_lengths[b0]) * w.kv_heads * w.head_dim * 4
+        desc = f"all {g} heads of sequence {b0}"
+    else:
+        heads = max(1, int(g * budget / t_seq))
+        kvh = w.kv_heads
+        heads = max(1, heads // (g // kvh)) * (g // kvh)  # whole GQA groups
+        heads = min(heads, g)
+        rows = np.arange(b0 * g, b0 * g + heads)
+        kv = int(w.context_lengths[b0]) * (heads // (g // kvh)) * w.head_dim * 4
+        desc = f"{heads} of {g} heads of sequence {b0}"
+    for _ in range(args.warmup):
+        oracle.decode(w, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(w, rows=rows)
+        times.append(time.perf_counter() - t0)
+    step = sum(times) / len(times)
+    value = kv / step / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "query_heads": w.query_heads,
+                       "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+                       "page_size": w.page_size, "sample_per_step": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"each step: {desc}"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

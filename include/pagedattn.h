@@ -1,0 +1,210 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn: paged decode attention on NVIDIA sm_103a (GB300).
+ *
+ * The operation ("[TIL] Optimizing paged attention", retepy.com, sections "Paged
+ * Attention", "Data Layout" and "Baseline"): a decode step gives every sequence b of a
+ * batch one query token with query_heads heads of head_dim elements. Its K/V history
+ * lives in a paged cache. Token t of sequence b is stored in physical page
+ * block_tables[b][t / page_size] at slot t % page_size. Query head h reads K/V head
+ * h / (query_heads / kv_heads), i.e. consecutive query heads share a K/V head (GQA).
+ * For each (b, h):
+ *
+ *     s_t    = scale * dot(query[b][h], key_cache[page(t)][slot(t)][kv(h)])   t < ctx[b]
+ *     out    = sum_t softmax(s)_t * value_cache[page(t)][slot(t)][kv(h)]
+ *
+ * Data types and layouts (all row-major, C order):
+ *   query          fp16  [batch][query_heads][head_dim]
+ *   key_cache      fp16  [num_physical_pages][page_size][kv_heads][head_dim]
+ *   value_cache    fp16  same layout as key_cache
+ *   block_tables   int32 [batch][max_pages_per_sequence]; only the first
+ *                        ceil(context_lengths[b] / page_size) entries of row b are read
+ *   context_lengths int32 [batch]
+ *   out            fp32  [batch][query_heads][head_dim]; fully overwritten
+ *
+ * Ownership: every pointer argument is device memory owned by the caller; the library
+ * neither retains nor frees it after the call returns. Calls are asynchronous on the
+ * given CUDA stream (a cudaStream_t passed as void*; NULL = the legacy default
+ * stream); no call synchronises the host or copies data to it, except
+ * pa_get_device_error. Results are deterministic: the same inputs on the same GPU model
+ * give bitwise-identical outputs (fixed work split, fixed merge order, no float atomics).
+ *
+ * Errors: host-side checks run before any launch and return a status without touching
+ * the GPU. Device-side index problems (a needed block-table entry outside
+ * [0, num_physical_pages), a context length outside [0, max_pages_per_sequence *
+ * page_size]) are never read through: the offending page is skipped, the context is
+ * clamped, and a flag is raised in the device error word (pa_get_device_error).
+ * A context length of 0 yields an all-zero output row.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Shape of one decode step. The pages' "Problem" (section "Baseline"), plus the size of
+ * the page pool so that page ids can be range-checked. */
+typedef struct pa_problem_t {
+  int32_t batch;                  /* sequences, >= 0 (0 is a no-op) */
+  int32_t query_heads;            /* >= 1, a multiple of kv_heads */
+  int32_t kv_heads;               /* >= 1 */
+  int32_t head_dim;               /* 64, 128 or 256 */
+  int32_t page_size;              /* tokens per page: a power of two in [8, 256] */
+  int32_t max_pages_per_sequence; /* columns of block_tables, >= 1 */
+  int32_t num_physical_pages;     /* pages in each cache, >= 1;
+                                     num_physical_pages * page_size < 2^31 */
+} pa_problem_t;
+
+typedef enum pa_status_t {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, query_heads % kv_heads != 0,
+                             non-finite scale, bad option value */
+  PA_ERR_UNSUPPORTED = 2, /* head_dim or page_size outside the supported set, pool too big */
+  PA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned (4 for int32 arrays) */
+  PA_ERR_WORKSPACE = 4,   /* caller workspace too small, or allocating it failed */
+  PA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
+  PA_ERR_NO_DEVICE = 6    /* no usable sm_103a device is current */
+} pa_status_t;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_PAGE_ID 1u /* a needed block-table entry was outside the page pool */
+#define PA_DEVERR_CONTEXT 2u /* a context length was < 0 or > max_pages*page_size */
+#define PA_DEVERR_TIMEOUT 4u /* a pipeline wait ran past its time limit; output invalid */
+
+/* How work is split across the GPU. */
+typedef enum pa_schedule_t {
+  PA_SCHEDULE_AUTO = 0,    /* heuristic (pa_plan) */
+  PA_SCHEDULE_SINGLE = 1,  /* one worker per (sequence, K/V head group), whole context,
+                              final output written directly; no workspace */
+  PA_SCHEDULE_BALANCED = 2 /* split-K: the concatenated K/V tiles of all sequences are cut
+                              into equal contiguous ranges, one per worker; a worker
+                              writes per-range (max, sum, partial output) for sequences it
+                              shares with other workers, and those are merged by
+                              log-sum-exp */
+} pa_schedule_t;
+
+/* Arithmetic of the group x token products. */
+typedef enum pa_math_t {
+  PA_MATH_AUTO = 0, /* heuristic (pa_plan) */
+  PA_MATH_SIMT = 1, /* fp32 FMA on CUDA cores */
+  PA_MATH_MMA = 2   /* fp16 x fp16 -> fp32 warp-level tensor-core tiles (m16n8k16) */
+} pa_math_t;
+
+/* Where the split-K merge runs (balanced schedule). */
+typedef enum pa_combine_t {
+  PA_COMBINE_FUSED = 0, /* the last worker to finish a sequence's head group merges it
+                           (one launch per call) */
+  PA_COMBINE_KERNEL = 1 /* a separate log-sum-exp combine kernel merges them */
+} pa_combine_t;
+
+typedef struct pa_options_t {
+  int32_t schedule;    /* pa_schedule_t */
+  int32_t math;        /* pa_math_t */
+  int32_t combine;     /* pa_combine_t */
+  int32_t workers;     /* balanced: number of workers (warps); 0 = as many as fit at once */
+  int32_t stages;      /* K/V pipeline depth per worker; 0 = default */
+  int32_t warps_per_cta; /* 0 = default */
+  int32_t reserved[2]; /* must be 0 */
+} pa_options_t;
+
+/* What pa_decode / pa_decode_ex will launch for a problem (filled by pa_plan). */
+typedef struct pa_plan_t {
+  int32_t schedule;       /* resolved pa_schedule_t */
+  int32_t math;           /* resolved pa_math_t */
+  int32_t combine;        /* resolved pa_combine_t */
+  int32_t workers;        /* warps that process K/V tiles */
+  int32_t warps_per_cta;
+  int32_t ctas;
+  int32_t stages;
+  int32_t tile_tokens;    /* tokens per K/V tile */
+  int32_t units;          /* batch * kv_heads * ceil(g / 8): (sequence, head group) units */
+  int32_t heads_per_unit; /* query heads one worker serves with one K/V read (<= 8) */
+  int64_t smem_bytes;     /* dynamic shared memory per CTA */
+  int64_t workspace_bytes;/* bytes pa_decode_ex needs for this plan */
+} pa_plan_t;
+
+/* Resolve the schedule/math heuristic for `problem` on a GPU with `sm_count` SMs.
+ * Pure host logic (no GPU needed). The heuristic follows the context-split discussion
+ * of the pages ("[TIL] Optimizing paged attention", section "V4 (Context-axis
+ * parallelism)"; partition sizing against the SM count in the paged_attention_v2
+ * notes): one worker per unit while the units alone fill the GPU several times over and
+ * the longest possible context (max_pages_per_sequence * page_size) is short; otherwise
+ * the balanced split-K schedule. options may be NULL (all AUTO). */
+pa_status_t pa_plan(const pa_problem_t *problem, const pa_options_t *options, int32_t sm_count,
+                    pa_plan_t *plan);
+
+/* Bytes of device workspace pa_decode_ex needs for `problem` and `options` on the current
+ * device (0 for the single-pass schedule). */
+pa_status_t pa_workspace_size(const pa_problem_t *problem, const pa_options_t *options,
+                              size_t *bytes);
+
+/* Zero a caller-owned workspace (cudaMemsetAsync on `stream`) and record that it is
+ * zero. Call it once for every new buffer (also when a freed buffer's address comes back
+ * from the allocator). Between calls the buffer must not be written by anyone else. A
+ * completed call leaves the merge counters it used at zero; the library remembers, per
+ * buffer address, how many are known to be zero and zeroes only the ones a later call with
+ * a larger problem adds (on that call's stream). After a call that raised
+ * PA_DEVERR_TIMEOUT, call pa_workspace_init again. */
+pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/* One decode step with the heuristic's plan. The split-K workspace, when needed, is
+ * owned by the library: one grow-only buffer per device, allocated on first need (the
+ * first call that needs it must not be inside stream capture), released at process
+ * exit. Calls that use that buffer must not overlap in time on different streams.
+ * query/key_cache/value_cache: fp16 device pointers; out: fp32 device pointer. */
+pa_status_t pa_decode(const pa_problem_t *problem, const void *query, const void *key_cache,
+                      const void *value_cache, const int32_t *block_tables,
+                      const int32_t *context_lengths, float scale, float *out, void *stream);
+
+/* pa_decode with explicit options and a caller-owned workspace of workspace_bytes
+ * (>= pa_workspace_size; zeroed once by pa_workspace_init). workspace may be NULL when
+ * the plan needs none. Concurrent calls must use distinct workspaces. */
+pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const void *key_cache,
+                         const void *value_cache, const int32_t *block_tables,
+                         const int32_t *context_lengths, float scale, float *out,
+                         const pa_options_t *options, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Split-K partial phase with a fixed number of splits per sequence, as in "[TIL]
+ * Optimizing paged attention", section "V4 (Context-axis parallelism)": sequence b's
+ * pages are cut into num_splits ranges of ceil(pages_b / num_splits) pages (the last
+ * ranges may be short or empty); for each (b, split, query head) it writes
+ *   partial_max [batch][num_splits][query_heads]           fp32: max_t s_t * log2(e)
+ *   partial_sum [batch][num_splits][query_heads]           fp32: sum_t 2^(s_t log2 e - max)
+ *   partial_out [batch][num_splits][query_heads][head_dim] fp32: sum_t 2^(..) * V_t,
+ *                                                          not normalised
+ * (an empty range writes max = -inf, sum = 0, out = 0). The maximum is in base-2 units
+ * (scores times log2(e)). num_splits >= 1. math: pa_math_t (0 = AUTO). */
+pa_status_t pa_split_kv_partial(const pa_problem_t *problem, const void *query,
+                                const void *key_cache, const void *value_cache,
+                                const int32_t *block_tables, const int32_t *context_lengths,
+                                float scale, int32_t num_splits, int32_t math,
+                                float *partial_max, float *partial_sum, float *partial_out,
+                                void *stream);
+
+/* Log-sum-exp combine of the arrays pa_split_kv_partial writes ("[TIL] Optimizing paged
+ * attention", section "V4 (Context-axis parallelism)", merge kernel): splits with sum 0
+ * are skipped, the rest are merged in split order and the result normalised into out
+ * [batch][query_heads][head_dim] (0 where every split is empty). */
+pa_status_t pa_split_kv_combine(const pa_problem_t *problem, int32_t num_splits,
+                                const float *partial_max, const float *partial_sum,
+                                const float *partial_out, float *out, void *stream);
+
+/* Read and clear the device error word of the current device (PA_DEVERR_* bits) after
+ * the work queued on `stream` finishes. Synchronises `stream`. */
+pa_status_t pa_get_device_error(void *stream, uint32_t *flags);
+
+/* Static description of a status code. */
+const char *pa_status_string(pa_status_t status);
+
+/* Library version as 10000 * major + 100 * minor + patch. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

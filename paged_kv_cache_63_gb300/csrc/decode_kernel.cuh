@@ -1,0 +1,901 @@
+// decode_kernel.cuh -- the paged decode attention kernel for sm_103a.
+//
+// Method ("[TIL] Optimizing paged attention", retepy.com): for each sequence b and query
+// head h, out = softmax(scale * q K^T) V over the sequence's context, where token t is at
+// physical page block_tables[b][t / page_size], slot t % page_size (sections "Data Layout"
+// and "Baseline"), the softmax is accumulated online (running max, rescaled sum and
+// accumulator; section "Baseline"), all query heads of a GQA group are served from one
+// K/V read (section "V3 (Shared memory data reuse)"), and long contexts are split across
+// workers whose (max, sum, partial output) states are merged by log-sum-exp (section
+// "V4 (Context-axis parallelism)").
+//
+// GB300 design:
+//  * A worker is one warp with a private ring of `stages` shared-memory K/V tiles of T
+//    tokens. Lane 0 issues TMA tensor loads (3-D map over [rows][kv_heads][head_dim],
+//    128-byte swizzle) for each page piece of a tile, one tile per mbarrier; the warp
+//    waits on the barrier, computes, and refills the slot S-1 tiles ahead. Warps never
+//    synchronise with each other.
+//  * Work units are (sequence, K/V head, head subgroup); a unit serves up to 8 query heads
+//    from one K/V read. Scores and the online softmax stay in fp32 registers, in base-2
+//    units (scale * log2 e folded in), with ex2.approx.
+//  * Math variants: SIMT (lanes over tokens for q.k, lanes over head_dim for p.V) and
+//    MMA (m16n8k16 fp16 tensor-core tiles: S[8 heads x 16 tokens] = Q K^T with K fragments
+//    by ldmatrix, then O += P V with the score fragments reused as the A operand and V
+//    fragments by ldmatrix.trans).
+//  * Schedules: SINGLE (a worker per unit), SPLIT (a worker per (unit, page range), the
+//    pages' fixed split) and BALANCED (the concatenated tiles of all units cut into one
+//    equal contiguous range per worker; a unit shared by several workers is merged by
+//    log-sum-exp, by the last of its workers or by a separate combine kernel).
+#pragma once
+
+#include <type_traits>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pa {
+
+template <int HD, int T>
+struct Geom {
+  static constexpr int kHalfBytes = T * HD * 2;  // the K (or V) part of a stage
+  static constexpr int kStageBytes = 2 * kHalfBytes;
+};
+
+// Byte offset of 16-byte chunk `chunk` (0 .. HD/8 - 1) of tile row `row`, as TMA lays a
+// [T rows][64 halves] box down with 128-byte swizzle: column block chunk / 8 is a
+// [T][128 B] array, and inside every 8-row group the chunk index is XORed with row & 7.
+template <int HD, int T>
+__device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * (T * 128) + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Context length of sequence b, clamped to [0, max_pages * page_size]; a value outside
+// that range raises PA_DEVERR_CONTEXT.
+__device__ __forceinline__ int load_ctx(const KernelArgs &a, int b) {
+  int c = __ldg(a.ctx + b);
+  const int cap = a.maxp << a.ps_shift;
+  if (c < 0 || c > cap) {
+    atomicOr(a.err, PA_DEVERR_CONTEXT);
+    c = c < 0 ? 0 : cap;
+  }
+  return c;
+}
+
+// Position of a worker in its token stream.
+struct Cursor {
+  int b;         // sequence
+  int us;        // unit within the sequence: kv_head * sub + subgroup
+  int tok;       // first token of the current tile
+  int end;       // exclusive token bound of the current unit segment
+  int left;      // tiles still to visit
+  long long ug0;  // balanced schedule: global index of the unit's first tile
+};
+
+// Balanced schedule: step to the next unit with at least one tile.
+__device__ __forceinline__ void next_unit(const KernelArgs &a, Cursor &c, int T) {
+  c.ug0 += tiles_of(c.end, T);
+  c.tok = 0;
+  if (++c.us == a.ups) {
+    c.us = 0;
+    do {
+      ++c.b;
+      c.end = (c.b < a.batch) ? load_ctx(a, c.b) : 1;
+    } while (c.b < a.batch && c.end == 0);
+  }
+}
+
+__device__ __forceinline__ void advance(const KernelArgs &a, Cursor &c, int T) {
+  c.tok += T;
+  --c.left;
+  if (a.mode == MODE_BALANCED && c.left > 0 && c.tok >= c.end) next_unit(a, c, T);
+}
+
+// Balanced schedule: total tiles over all units, the number of workers that get tiles
+// (min(workers, total), so that every such worker's range is non-empty and the workers
+// sharing a unit are consecutive), and the cursor at this worker's first tile. Returns
+// false when the worker gets no tiles.
+__device__ inline bool balanced_start(const KernelArgs &a, int worker, int T, Cursor &c,
+                                      long long &total, long long &nworkers) {
+  const int lane = threadIdx.x & 31;
+  long long tiles = 0;
+  for (int base = 0; base < a.batch; base += 32) {
+    const int b = base + lane;
+    const int t = b < a.batch ? tiles_of(load_ctx(a, b), T) : 0;
+    tiles += warp_sum(static_cast<long long>(t));
+  }
+  total = tiles * a.ups;
+  nworkers = total < a.workers ? total : a.workers;
+  if (worker >= nworkers) return false;
+  const long long s = worker_start(worker, total, nworkers);
+  const long long e = worker_start(worker + 1, total, nworkers);
+  long long run = 0;
+  for (int base = 0; base < a.batch; base += 32) {
+    const int b = base + lane;
+    const long long t =
+        b < a.batch ? static_cast<long long>(tiles_of(load_ctx(a, b), T)) * a.ups : 0;
+    long long incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const long long chunk = __shfl_sync(0xffffffffu, incl, 31);
+    if (s < run + chunk) {
+      const unsigned m = __ballot_sync(0xffffffffu, run + incl > s);
+      const int L = __ffs(m) - 1;
+      const long long excl = __shfl_sync(0xffffffffu, incl - t, L);
+      c.b = base + L;
+      c.end = load_ctx(a, c.b);
+      const int tb = tiles_of(c.end, T);
+      const long long inner = s - (run + excl);
+      c.us = static_cast<int>(inner / tb);
+      c.tok = static_cast<int>(inner % tb) * T;
+      c.ug0 = run + excl + static_cast<long long>(c.us) * tb;
+      c.left = static_cast<int>(e - s);
+      return true;
+    }
+    run += chunk;
+  }
+  return false;
+}
+
+// A 64-entry window of one sequence's block-table row, held one entry per lane in two
+// registers (entries base..base+31 and base+32..base+63); the second half is loaded one
+// window ahead so the TMA issue rarely waits on a block-table read. Entries at or past
+// `npages` (the pages the context needs) are never read.
+struct BtWindow {
+  int b, base, cur, nxt;
+};
+
+__device__ __forceinline__ int bt_load(const KernelArgs &a, int b, int lp, int npages) {
+  return lp < npages ? __ldg(a.bt + static_cast<long long>(b) * a.maxp + lp) : -1;
+}
+
+__device__ __forceinline__ int bt_page(const KernelArgs &a, BtWindow &w, int b, int lp,
+                                       int npages) {
+  const int lane = threadIdx.x & 31;
+  if (b != w.b || lp < w.base || lp >= w.base + 64) {
+    w.b = b;
+    w.base = lp & ~31;
+    w.cur = bt_load(a, b, w.base + lane, npages);
+    w.nxt = bt_load(a, b, w.base + 32 + lane, npages);
+  } else if (lp >= w.base + 32) {
+    w.base += 32;
+    w.cur = w.nxt;
+    w.nxt = bt_load(a, b, w.base + 32 + lane, npages);
+  }
+  return __shfl_sync(0xffffffffu, w.cur, lp - w.base);
+}
+
+// Issue the TMA loads of the tile at cursor c into a stage (warp-uniform call).
+template <int HD, int T>
+__device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMap *tk,
+                                           const CUtensorMap *tv, const Cursor &c,
+                                           BtWindow &w, uint32_t stage, uint32_t bar,
+                                           uint64_t pol) {
+  constexpr int kMaxPieces = T / 8;
+  const int R = a.ps < T ? a.ps : T;  // rows per piece: a piece never crosses a page
+  const int pieces = T / R;
+  const int kv = c.us / a.sub;
+  const int npages = (c.end + a.ps - 1) >> a.ps_shift;
+  int row[kMaxPieces];
+  uint32_t bytes = 0;
+#pragma unroll
+  for (int p = 0; p < kMaxPieces; ++p) {
+    row[p] = -1;
+    const int tok = c.tok + p * R;
+    if (p < pieces && tok < c.end) {
+      const int page = bt_page(a, w, c.b, tok >> a.ps_shift, npages);
+      if (page < 0 || page >= a.num_pages) {
+        if ((threadIdx.x & 31) == 0) atomicOr(a.err, PA_DEVERR_PAGE_ID);
+      } else {
+        row[p] = (page << a.ps_shift) + (tok & (a.ps - 1));
+        bytes += static_cast<uint32_t>(R * HD * 4);
+      }
+    }
+  }
+  if ((threadIdx.x & 31) == 0) {
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int p = 0; p < kMaxPieces; ++p) {
+      if (row[p] < 0) continue;
+#pragma unroll
+      for (int blk = 0; blk < HD / 64; ++blk) {
+        const uint32_t dst = stage + blk * (T * 128) + p * R * 128;
+        tma_load_3d(dst, tk, bar, blk * 64, kv, row[p], pol);
+        tma_load_3d(dst + Geom<HD, T>::kHalfBytes, tv, bar, blk * 64, kv, row[p], pol);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ SIMT arithmetic
+template <int HD, int NH>
+struct SimtState {
+  static constexpr int DPL = HD / 32;
+  float m[NH], lsum[NH];
+  float acc[NH][DPL];
+};
+
+template <int NH>
+struct Nhp {
+  static constexpr int v = (NH + 3) & ~3;
+};
+
+template <int HD, int NH>
+__device__ __forceinline__ void simt_begin(SimtState<HD, NH> &st, const KernelArgs &a, int b,
+                                           int h0, int nh, uint32_t qs) {
+  const int lane = threadIdx.x & 31;
+  const uint16_t *src = a.q + (static_cast<long long>(b) * a.qh + h0) * HD;
+  for (int i = lane; i < NH * HD / 8; i += 32) {
+    const int h = i / (HD / 8);
+    const int d8 = i % (HD / 8);
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = 0.f;
+    if (h < nh) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(src + h * HD + d8 * 8));
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 v = half2_bits_to_float2(w4[j]);
+        f[2 * j] = v.x * a.scale_log2;
+        f[2 * j + 1] = v.y * a.scale_log2;
+      }
+    }
+    const uint32_t dst = qs + (h * HD + d8 * 8) * 4;
+    sts128(dst, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                           __float_as_uint(f[3])));
+    sts128(dst + 16, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                __float_as_uint(f[6]), __float_as_uint(f[7])));
+  }
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    st.m[h] = -INFINITY;
+    st.lsum[h] = 0.f;
+#pragma unroll
+    for (int i = 0; i < SimtState<HD, NH>::DPL; ++i) st.acc[h][i] = 0.f;
+  }
+}
+
+template <int HD, int T, int NH>
+__device__ __forceinline__ void simt_tile(SimtState<HD, NH> &st, uint32_t stk, uint32_t qs,
+                                          uint32_t pbuf, int tok0, int end) {
+  constexpr int LPT = 32 / T;  // lanes per token in the score phase
+  constexpr int CH = HD / LPT / 8;  // 16-byte chunks of a row per lane
+  constexpr int DPL = HD / 32;
+  constexpr int NHP = Nhp<NH>::v;
+  const int lane = threadIdx.x & 31;
+  const int r = lane % T;
+  const int part = lane / T;
+  const uint32_t stv = stk + Geom<HD, T>::kHalfBytes;
+
+  // scores: lane (r, part) dots its share of K row r with every head's scaled q
+  float s[NH];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) s[h] = 0.f;
+#pragma unroll 2
+  for (int c = 0; c < CH; ++c) {
+    const int chunk = part * CH + c;
+    const uint4 raw = lds128(stk + tile_off<HD, T>(r, chunk));
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    float kf[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 v = half2_bits_to_float2(w4[j]);
+      kf[2 * j] = v.x;
+      kf[2 * j + 1] = v.y;
+    }
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const uint4 q0 = lds128(qs + (h * HD + chunk * 8) * 4);
+      const uint4 q1 = lds128(qs + (h * HD + chunk * 8) * 4 + 16);
+      float t = s[h];
+      t = fmaf(kf[0], __uint_as_float(q0.x), t);
+      t = fmaf(kf[1], __uint_as_float(q0.y), t);
+      t = fmaf(kf[2], __uint_as_float(q0.z), t);
+      t = fmaf(kf[3], __uint_as_float(q0.w), t);
+      t = fmaf(kf[4], __uint_as_float(q1.x), t);
+      t = fmaf(kf[5], __uint_as_float(q1.y), t);
+      t = fmaf(kf[6], __uint_as_float(q1.z), t);
+      t = fmaf(kf[7], __uint_as_float(q1.w), t);
+      s[h] = t;
+    }
+  }
+  if (LPT == 2) {
+#pragma unroll
+    for (int h = 0; h < NH; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], 16);
+  }
+
+  // online softmax (base 2): tile max, rescale factor, probabilities
+  const bool valid = tok0 + r < end;
+  float alpha[NH];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const float x = valid ? s[h] : -INFINITY;
+    float mt = x;
+#pragma unroll
+    for (int o = T / 2; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+    const float mn = fmaxf(st.m[h], mt);
+    alpha[h] = fast_exp2(st.m[h] - mn);
+    st.m[h] = mn;
+    const float p = fast_exp2(x - mn);
+    st.lsum[h] = st.lsum[h] * alpha[h] + (lane < T ? p : 0.f);
+    s[h] = p;
+  }
+  if (lane < T) {
+#pragma unroll
+    for (int h = 0; h < NHP; h += 4) {
+      const float p0 = s[h];
+      const float p1 = (h + 1 < NH) ? s[h + 1] : 0.f;
+      const float p2 = (h + 2 < NH) ? s[h + 2] : 0.f;
+      const float p3 = (h + 3 < NH) ? s[h + 3] : 0.f;
+      sts128(pbuf + (r * NHP + h) * 4, make_uint4(__float_as_uint(p0), __float_as_uint(p1),
+                                                  __float_as_uint(p2), __float_as_uint(p3)));
+    }
+  }
+  __syncwarp();
+
+  // values: lane owns DPL consecutive dims; rows past `end` are never read
+#pragma unroll
+  for (int h = 0; h < NH; ++h)
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) st.acc[h][i] *= alpha[h];
+  const int nvalid = min(T, end - tok0);
+  const int d0 = lane * DPL;
+  const uint32_t vcol = static_cast<uint32_t>((d0 & 7) * 2);
+#pragma unroll 4
+  for (int rr = 0; rr < nvalid; ++rr) {
+    const uint32_t va = stv + tile_off<HD, T>(rr, d0 >> 3) + vcol;
+    float vf[DPL];
+    if constexpr (DPL == 8) {
+      const uint4 raw = lds128(va);
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 v = half2_bits_to_float2(w4[j]);
+        vf[2 * j] = v.x;
+        vf[2 * j + 1] = v.y;
+      }
+    } else if constexpr (DPL == 4) {
+      const uint2 raw = lds64(va);
+      const float2 v0 = half2_bits_to_float2(raw.x);
+      const float2 v1 = half2_bits_to_float2(raw.y);
+      vf[0] = v0.x;
+      vf[1] = v0.y;
+      vf[2] = v1.x;
+      vf[3] = v1.y;
+    } else {
+      const float2 v0 = half2_bits_to_float2(lds32(va));
+      vf[0] = v0.x;
+      vf[1] = v0.y;
+    }
+#pragma unroll
+    for (int h = 0; h < NHP; h += 4) {
+      const uint4 p4 = lds128(pbuf + (rr * NHP + h) * 4);
+      const float pv[4] = {__uint_as_float(p4.x), __uint_as_float(p4.y), __uint_as_float(p4.z),
+                           __uint_as_float(p4.w)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (h + j < NH) {
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) st.acc[h + j][i] = fmaf(pv[j], vf[i], st.acc[h + j][i]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA arithmetic
+template <int HD>
+struct MmaState {
+  float m, lsum;          // row (head) lane / 4
+  float o[HD / 8][2];     // O[lane / 4][8 nt + 2 (lane % 4) + {0, 1}]
+  uint32_t qa[HD / 16][2];  // A fragments of q: rows 0..7, k = 16 ks + 2 (lane % 4) (+8)
+};
+
+template <int HD>
+__device__ __forceinline__ void mma_begin(MmaState<HD> &st, const KernelArgs &a, int b, int h0,
+                                          int nh) {
+  const int lane = threadIdx.x & 31;
+  const int h = lane >> 2;
+  const int c = (lane & 3) * 2;
+  const uint32_t *src =
+      reinterpret_cast<const uint32_t *>(a.q + (static_cast<long long>(b) * a.qh + h0 + h) * HD);
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks) {
+    st.qa[ks][0] = h < nh ? __ldg(src + (ks * 16 + c) / 2) : 0u;
+    st.qa[ks][1] = h < nh ? __ldg(src + (ks * 16 + 8 + c) / 2) : 0u;
+  }
+  st.m = -INFINITY;
+  st.lsum = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < HD / 8; ++nt) st.o[nt][0] = st.o[nt][1] = 0.f;
+}
+
+// Zero V rows [from, T) of a stage (all chunks), so that a zero probability can never
+// meet a non-finite value left in an unused row.
+template <int HD, int T>
+__device__ __forceinline__ void zero_v_rows(uint32_t stv, int from) {
+  const int lane = threadIdx.x & 31;
+  const int n = (T - from) * (HD / 8);
+  for (int i = lane; i < n; i += 32) {
+    const int row = from + i / (HD / 8);
+    const int chunk = i % (HD / 8);
+    sts128(stv + (chunk >> 3) * (T * 128) + row * 128 + (chunk & 7) * 16, make_uint4(0, 0, 0, 0));
+  }
+}
+
+template <int HD, int T>
+__device__ __forceinline__ void mma_tile(MmaState<HD> &st, uint32_t stk, int tok0, int end,
+                                         float scale_log2) {
+  constexpr int NCH = T / 16;
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3;
+  const int rr = lane & 7;
+  const uint32_t stv = stk + Geom<HD, T>::kHalfBytes;
+
+  // S[h][t] for the tile's 16-token chunks: two n8 tiles per chunk
+  float sc[NCH][2][2];
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    sc[ch][0][0] = sc[ch][0][1] = sc[ch][1][0] = sc[ch][1][1] = 0.f;
+    const int krow = ch * 16 + (mi >> 1) * 8 + rr;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(stk + tile_off<HD, T>(krow, ks * 2 + (mi & 1)), b0, b1, b2, b3);
+      mma_rows8(sc[ch][0][0], sc[ch][0][1], st.qa[ks][0], st.qa[ks][1], b0, b1);
+      mma_rows8(sc[ch][1][0], sc[ch][1][1], st.qa[ks][0], st.qa[ks][1], b2, b3);
+    }
+  }
+
+  // online softmax (base 2) for row lane / 4: the row's 16 * NCH scores live in the 4
+  // lanes lane & ~3 .. lane | 3
+  float mt = -INFINITY;
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = tok0 + ch * 16 + nt * 8 + 2 * (lane & 3) + j;
+        const float x = tok < end ? sc[ch][nt][j] * scale_log2 : -INFINITY;
+        sc[ch][nt][j] = x;
+        mt = fmaxf(mt, x);
+      }
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+  const float mn = fmaxf(st.m, mt);
+  const float alpha = fast_exp2(st.m - mn);
+  st.m = mn;
+  float psum = 0.f;
+  uint32_t pa[NCH][2];
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float p0 = fast_exp2(sc[ch][nt][0] - mn);
+      const float p1 = fast_exp2(sc[ch][nt][1] - mn);
+      psum += p0 + p1;
+      pa[ch][nt] = pack_half2(p0, p1);
+    }
+  st.lsum = st.lsum * alpha + psum;
+#pragma unroll
+  for (int nt = 0; nt < HD / 8; ++nt) {
+    st.o[nt][0] *= alpha;
+    st.o[nt][1] *= alpha;
+  }
+
+  const int nvalid = end - tok0;
+  if (nvalid < T) {
+    zero_v_rows<HD, T>(stv, nvalid);
+    __syncwarp();
+  }
+#pragma unroll
+  for (int ch = 0; ch < NCH; ++ch) {
+    const int vrow = ch * 16 + (mi & 1) * 8 + rr;
+#pragma unroll
+    for (int dt = 0; dt < HD / 16; ++dt) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_trans(stv + tile_off<HD, T>(vrow, dt * 2 + (mi >> 1)), b0, b1, b2, b3);
+      mma_rows8(st.o[2 * dt][0], st.o[2 * dt][1], pa[ch][0], pa[ch][1], b0, b1);
+      mma_rows8(st.o[2 * dt + 1][0], st.o[2 * dt + 1][1], pa[ch][0], pa[ch][1], b2, b3);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ merge (log-sum-exp)
+// Merge n partial states of one unit (balanced layout, slots unit + c0 .. unit + c0 + n - 1,
+// in that order) into normalised rows of `out`; lanes own head_dim / 32 dims.
+template <int HD>
+__device__ __forceinline__ void merge_balanced(const KernelArgs &a, long long unit, long long c0,
+                                               int n, int b, int h0, int nh) {
+  constexpr int DPL = HD / 32;
+  const int lane = threadIdx.x & 31;
+  for (int h = 0; h < nh; ++h) {
+    float M = -INFINITY, L = 0.f;
+    float O[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) O[i] = 0.f;
+    for (int k = 0; k < n; ++k) {
+      const long long slot = slot_of(unit, c0 + k);
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
+      if (ml.y == 0.f) continue;
+      const float Mn = fmaxf(M, ml.x);
+      const float al = fast_exp2(M - Mn);
+      const float be = fast_exp2(ml.x - Mn);
+      L = al * L + be * ml.y;
+      const float *src = a.ws_acc + (slot * kMaxHeads + h) * HD + lane * DPL;
+#pragma unroll
+      for (int i = 0; i < DPL; i += 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
+        O[i] = al * O[i] + be * v.x;
+        O[i + 1] = al * O[i + 1] + be * v.y;
+      }
+      M = Mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    float *dst = a.out + (static_cast<long long>(b) * a.qh + h0 + h) * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2)
+      *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
+  }
+}
+
+// Unit coordinates.
+struct UnitInfo {
+  int b, us, h0, nh;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const KernelArgs &a, int b, int us) {
+  UnitInfo u;
+  u.b = b;
+  u.us = us;
+  const int k = us / a.sub;
+  const int sg = us % a.sub;
+  u.h0 = k * a.g + sg * a.nh_unit;
+  u.nh = min(a.nh_unit, a.g - sg * a.nh_unit);
+  return u;
+}
+
+// Writes of one finished unit segment. `whole`: this worker saw the unit's full context;
+// otherwise a partial state goes to `slot` (balanced) or to split `split` (fixed split).
+template <int HD, bool MMA, int NH>
+struct Epilogue;
+
+template <int HD, int NH>
+struct Epilogue<HD, true, NH> {
+  template <typename St>
+  __device__ static void final_out(const KernelArgs &a, St &st, const UnitInfo &u) {
+    const int lane = threadIdx.x & 31;
+    float l = st.lsum;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int h = lane >> 2;
+    if (h >= u.nh) return;
+    const float inv = 1.f / l;
+    float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0 + h) * HD + 2 * (lane & 3);
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; ++nt)
+      *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(st.o[nt][0] * inv, st.o[nt][1] * inv);
+  }
+  // Partial state to (max, sum, acc) arrays with per-head strides.
+  template <typename St>
+  __device__ static void partial_out(St &st, const UnitInfo &u, float *mx, float *sm, float *acc,
+                                     long long head_stride_ml, long long head_stride_acc) {
+    const int lane = threadIdx.x & 31;
+    float l = st.lsum;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const int h = lane >> 2;
+    if (h >= u.nh) return;
+    if ((lane & 3) == 0) {
+      mx[h * head_stride_ml] = st.m;
+      sm[h * head_stride_ml] = l;
+    }
+    float *dst = acc + h * head_stride_acc + 2 * (lane & 3);
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; ++nt)
+      *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(st.o[nt][0], st.o[nt][1]);
+  }
+};
+
+template <int HD, int NH>
+struct Epilogue<HD, false, NH> {
+  static constexpr int DPL = HD / 32;
+  template <typename St>
+  __device__ static void final_out(const KernelArgs &a, St &st, const UnitInfo &u) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float l = warp_sum(st.lsum[h]);
+      if (h < u.nh) {
+        const float inv = 1.f / l;
+        float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0 + h) * HD + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; i += 2)
+          *reinterpret_cast<float2 *>(dst + i) = make_float2(st.acc[h][i] * inv, st.acc[h][i + 1] * inv);
+      }
+    }
+  }
+  template <typename St>
+  __device__ static void partial_out(St &st, const UnitInfo &u, float *mx, float *sm, float *acc,
+                                     long long head_stride_ml, long long head_stride_acc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const float l = warp_sum(st.lsum[h]);
+      if (h < u.nh) {
+        if (lane == 0) {
+          mx[h * head_stride_ml] = st.m[h];
+          sm[h * head_stride_ml] = l;
+        }
+        float *dst = acc + h * head_stride_acc + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; i += 2)
+          *reinterpret_cast<float2 *>(dst + i) = make_float2(st.acc[h][i], st.acc[h][i + 1]);
+      }
+    }
+  }
+};
+
+// Zero the output rows of a unit (a context of length 0).
+template <int HD>
+__device__ __forceinline__ void zero_unit(const KernelArgs &a, const UnitInfo &u) {
+  const int lane = threadIdx.x & 31;
+  float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0) * HD;
+  for (int i = lane * 2; i < u.nh * HD; i += 64) *reinterpret_cast<float2 *>(dst + i) = make_float2(0.f, 0.f);
+}
+
+template <int HD, int T, bool MMA, int NH>
+__global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
+    decode_kernel(const __grid_constant__ KernelArgs a, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv) {
+  using G = Geom<HD, T>;
+  using Ep = Epilogue<HD, MMA, NH>;
+  extern __shared__ uint8_t dsm[];
+  __shared__ __align__(8) uint64_t bars[kMaxWarpsPerCta * kMaxStages];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int worker = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int S = a.stages;
+  const uint32_t wbase =
+      ((smem_addr(dsm) + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1)) +
+      warp * a.warp_smem;
+  const uint32_t qs = wbase + S * G::kStageBytes;  // SIMT: scaled q, fp32 [NH][HD]
+  const uint32_t pbuf = qs + NH * HD * 4;           // SIMT: probabilities [T][NHP]
+  const uint32_t bar0 = smem_addr(&bars[warp * kMaxStages]);
+
+  // ---- the worker's range
+  Cursor c;
+  long long total = 0, nworkers = 0;
+  const int units = a.batch * a.ups;
+  if (a.mode == MODE_BALANCED) {
+    if (worker >= a.workers) return;
+    const bool any = balanced_start(a, worker, T, c, total, nworkers);
+    // sequences with an empty context: zero their rows (worker b mod workers)
+    for (int b = worker; b < a.batch; b += a.workers) {
+      if (load_ctx(a, b) != 0) continue;
+      for (int us = 0; us < a.ups; ++us) {
+        zero_unit<HD>(a, unit_info(a, b, us));
+        if (!a.fused && lane == 0) {
+          a.ws_info[2 * (b * a.ups + us)] = 0;
+          a.ws_info[2 * (b * a.ups + us) + 1] = 0;
+        }
+      }
+    }
+    if (!any) return;
+  } else if (a.mode == MODE_SINGLE) {
+    if (worker >= units) return;
+    c.b = worker / a.ups;
+    c.us = worker % a.ups;
+    c.end = load_ctx(a, c.b);
+    c.tok = 0;
+    c.left = tiles_of(c.end, T);
+    c.ug0 = 0;
+    if (c.left == 0) {
+      zero_unit<HD>(a, unit_info(a, c.b, c.us));
+      return;
+    }
+  } else {  // MODE_SPLIT
+    if (worker >= units * a.num_splits) return;
+    const int u = worker / a.num_splits;
+    const int sp = worker % a.num_splits;
+    c.b = u / a.ups;
+    c.us = u % a.ups;
+    const int ctx = load_ctx(a, c.b);
+    const int pages = (ctx + a.ps - 1) >> a.ps_shift;
+    const int pps = (pages + a.num_splits - 1) / a.num_splits;
+    const int p0 = min(sp * pps, pages);
+    const int p1 = min(p0 + pps, pages);
+    c.tok = p0 << a.ps_shift;
+    c.end = min(p1 << a.ps_shift, ctx);
+    c.left = c.end > c.tok ? tiles_of(c.end - c.tok, T) : 0;
+    c.ug0 = 0;
+    if (c.left == 0) {
+      const UnitInfo ui = unit_info(a, c.b, c.us);
+      const long long row = (static_cast<long long>(c.b) * a.num_splits + sp) * a.qh + ui.h0;
+      for (int h = 0; h < ui.nh; ++h) {
+        if (lane == 0) {
+          a.p_max[row + h] = -INFINITY;
+          a.p_sum[row + h] = 0.f;
+        }
+        for (int i = lane * 2; i < HD; i += 64)
+          *reinterpret_cast<float2 *>(a.p_out + (row + h) * HD + i) = make_float2(0.f, 0.f);
+      }
+      return;
+    }
+  }
+
+  // ---- pipeline set-up
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  __syncwarp();
+  const uint64_t pol = l2_evict_first_policy();
+
+  Cursor ic = c;
+  BtWindow win;
+  win.b = -1;
+  win.base = 0;
+  win.cur = win.nxt = -1;
+  int issued = 0, consumed = 0;
+  for (; issued < S - 1 && ic.left > 0; ++issued) {
+    issue_tile<HD, T>(a, &tk, &tv, ic, win, wbase + issued * G::kStageBytes, bar0 + 8 * issued, pol);
+    advance(a, ic, T);
+  }
+
+  typename std::conditional<MMA, MmaState<HD>, SimtState<HD, NH>>::type st;
+  UnitInfo cur;
+  cur.b = -1;
+  cur.us = -1;
+  cur.h0 = cur.nh = 0;
+  long long cur_ug0 = 0;
+  int cur_end = 0;
+  bool aborted = false;
+
+  auto finish_unit = [&]() {
+    if (a.mode == MODE_SINGLE) {
+      Ep::final_out(a, st, cur);
+      return;
+    }
+    if (a.mode == MODE_SPLIT) {
+      const int sp = worker % a.num_splits;
+      const long long row = (static_cast<long long>(cur.b) * a.num_splits + sp) * a.qh + cur.h0;
+      Ep::partial_out(st, cur, a.p_max + row, a.p_sum + row, a.p_out + row * HD, 1, HD);
+      return;
+    }
+    const long long unit = static_cast<long long>(cur.b) * a.ups + cur.us;
+    const int nt = tiles_of(cur_end, T);
+    const long long c0 = worker_of(cur_ug0, total, nworkers);
+    const long long c1 = worker_of(cur_ug0 + nt - 1, total, nworkers);
+    const int n = static_cast<int>(c1 - c0 + 1);
+    if (!a.fused && worker == c0 && lane == 0) {
+      a.ws_info[2 * unit] = static_cast<int>(c0);
+      a.ws_info[2 * unit + 1] = n;
+    }
+    if (n == 1) {
+      Ep::final_out(a, st, cur);
+      return;
+    }
+    const long long slot = slot_of(unit, worker);
+    Ep::partial_out(st, cur, a.ws_ml + slot * kMaxHeads * 2, a.ws_ml + slot * kMaxHeads * 2 + 1,
+                    a.ws_acc + slot * kMaxHeads * HD, 2, HD);
+    if (!a.fused) return;
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(a.ws_count + unit, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old == n - 1) {
+      __threadfence();
+      merge_balanced<HD>(a, unit, c0, n, cur.b, cur.h0, cur.nh);
+      if (lane == 0) atomicExch(a.ws_count + unit, 0);
+    }
+  };
+
+  // ---- main loop: refill the slot freed last iteration, wait for the next tile, compute
+  while (c.left > 0) {
+    if (c.b != cur.b || c.us != cur.us) {
+      if (cur.b >= 0) finish_unit();
+      cur = unit_info(a, c.b, c.us);
+      cur_ug0 = c.ug0;
+      cur_end = c.end;
+      if constexpr (MMA)
+        mma_begin<HD>(st, a, cur.b, cur.h0, cur.nh);
+      else
+        simt_begin<HD, NH>(st, a, cur.b, cur.h0, cur.nh, qs);
+    }
+    if (ic.left > 0) {
+      const int s = issued % S;
+      issue_tile<HD, T>(a, &tk, &tv, ic, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol);
+      ++issued;
+      advance(a, ic, T);
+    }
+    const int s = consumed % S;
+    if (!mbar_wait(bar0 + 8 * s, static_cast<uint32_t>((consumed / S) & 1), a.err)) {
+      aborted = true;
+      break;
+    }
+    const uint32_t stk = wbase + s * G::kStageBytes;
+    if constexpr (MMA)
+      mma_tile<HD, T>(st, stk, c.tok, c.end, a.scale_log2);
+    else
+      simt_tile<HD, T, NH>(st, stk, qs, pbuf, c.tok, c.end);
+    fence_proxy_async();
+    __syncwarp();
+    ++consumed;
+    advance(a, c, T);
+  }
+  if (aborted) {
+    // let the copies still in flight land before the shared memory is given up
+    for (int i = consumed; i < issued; ++i)
+      mbar_wait(bar0 + 8 * (i % S), static_cast<uint32_t>((i / S) & 1), a.err);
+    return;
+  }
+  finish_unit();
+}
+
+// Separate log-sum-exp combine for the balanced schedule: one warp per unit.
+template <int HD>
+__global__ void __launch_bounds__(256) combine_balanced_kernel(const __grid_constant__ KernelArgs a) {
+  const long long unit = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (unit >= static_cast<long long>(a.batch) * a.ups) return;
+  const int c0 = a.ws_info[2 * unit];
+  const int n = a.ws_info[2 * unit + 1];
+  if (n <= 1) return;
+  const UnitInfo u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
+  merge_balanced<HD>(a, unit, c0, n, u.b, u.h0, u.nh);
+}
+
+// Log-sum-exp combine of the fixed-split arrays: one warp per (sequence, query head).
+template <int HD>
+__global__ void __launch_bounds__(256) combine_split_kernel(const __grid_constant__ KernelArgs a) {
+  constexpr int DPL = HD / 32;
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (row >= static_cast<long long>(a.batch) * a.qh) return;
+  const int lane = threadIdx.x & 31;
+  const long long b = row / a.qh;
+  const long long h = row % a.qh;
+  float M = -INFINITY, L = 0.f;
+  float O[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) O[i] = 0.f;
+  for (int s = 0; s < a.num_splits; ++s) {
+    const long long idx = (b * a.num_splits + s) * a.qh + h;
+    const float l = __ldg(a.p_sum + idx);
+    if (l == 0.f) continue;
+    const float m = __ldg(a.p_max + idx);
+    const float Mn = fmaxf(M, m);
+    const float al = fast_exp2(M - Mn);
+    const float be = fast_exp2(m - Mn);
+    L = al * L + be * l;
+    const float *src = a.p_out + idx * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2) {
+      const float2 v = __ldg(reinterpret_cast<const float2 *>(src + i));
+      O[i] = al * O[i] + be * v.x;
+      O[i + 1] = al * O[i + 1] + be * v.y;
+    }
+    M = Mn;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float *dst = a.out + row * HD + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; i += 2) *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
+}
+
+}  // namespace pa

@@ -1,0 +1,83 @@
+// decode_launch.cuh -- host-side launchers of the decode and combine kernels for one
+// head_dim; each decode_hd*.cu instantiates them for its head_dim.
+#pragma once
+
+#include "decode_kernel.cuh"
+
+namespace pa {
+
+template <int HD>
+constexpr int kTileTokens = HD >= 256 ? 16 : 32;
+
+constexpr int kMaxDevices = 64;
+
+template <int HD, bool MMA, int NH>
+cudaError_t launch_variant(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                           int ctas, int warps, size_t smem, cudaStream_t stream) {
+  auto kern = decode_kernel<HD, kTileTokens<HD>, MMA, NH>;
+  // the opt-in shared-memory size is a per-device function attribute; remember the
+  // largest value set on each device
+  static int smem_set[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || smem_set[dev] < static_cast<int>(smem)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) smem_set[dev] = static_cast<int>(smem);
+  }
+  kern<<<ctas, warps * 32, smem, stream>>>(a, *tk, *tv);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_decode_hd(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                             int mma, int nh_inst, int ctas, int warps, size_t smem,
+                             cudaStream_t stream) {
+  if (mma) return launch_variant<HD, true, kMaxHeads>(a, tk, tv, ctas, warps, smem, stream);
+  switch (nh_inst) {
+    case 1: return launch_variant<HD, false, 1>(a, tk, tv, ctas, warps, smem, stream);
+    case 2: return launch_variant<HD, false, 2>(a, tk, tv, ctas, warps, smem, stream);
+    case 4: return launch_variant<HD, false, 4>(a, tk, tv, ctas, warps, smem, stream);
+    case 6: return launch_variant<HD, false, 6>(a, tk, tv, ctas, warps, smem, stream);
+    case 8: return launch_variant<HD, false, 8>(a, tk, tv, ctas, warps, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int HD>
+cudaError_t launch_combine_balanced_hd(const KernelArgs &a, int units, cudaStream_t stream) {
+  const long long threads = static_cast<long long>(units) * 32;
+  const int blocks = static_cast<int>((threads + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  combine_balanced_kernel<HD><<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_combine_split_hd(const KernelArgs &a, cudaStream_t stream) {
+  const long long threads = static_cast<long long>(a.batch) * a.qh * 32;
+  const int blocks = static_cast<int>((threads + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  combine_split_kernel<HD><<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa
+
+#define PA_INSTANTIATE_HD(HD)                                                                \
+  namespace pa {                                                                             \
+  cudaError_t launch_decode_hd##HD(const KernelArgs &a, const CUtensorMap *tk,               \
+                                   const CUtensorMap *tv, int mma, int nh_inst, int ctas,    \
+                                   int warps, size_t smem, cudaStream_t stream) {            \
+    return launch_decode_hd<HD>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);         \
+  }                                                                                          \
+  cudaError_t launch_combine_balanced_hd##HD(const KernelArgs &a, int units,                 \
+                                             cudaStream_t stream) {                          \
+    return launch_combine_balanced_hd<HD>(a, units, stream);                                 \
+  }                                                                                          \
+  cudaError_t launch_combine_split_hd##HD(const KernelArgs &a, cudaStream_t stream) {        \
+    return launch_combine_split_hd<HD>(a, stream);                                           \
+  }                                                                                          \
+  }

@@ -1,0 +1,97 @@
+// internal.h -- types shared by the host API (api.cpp) and the kernel launchers (*.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define PA_HD __host__ __device__ __forceinline__
+#else
+#define PA_HD inline
+#endif
+
+namespace pa {
+
+// Query heads one worker serves from one K/V read; a group larger than this is split
+// into ceil(g / kMaxHeads) units that each read the group's K/V.
+constexpr int kMaxHeads = 8;
+constexpr int kMaxWarpsPerCta = 8;
+constexpr int kMaxStages = 8;
+constexpr int kSmemAlign = 1024;  // 128-byte TMA swizzle repeats every 1024 bytes
+
+enum Mode : int {
+  MODE_SINGLE = 0,   // one worker per unit, whole context, final output
+  MODE_SPLIT = 1,    // one worker per (unit, split): fixed page ranges, partial arrays
+  MODE_BALANCED = 2  // equal contiguous ranges of the concatenated tiles, merge by LSE
+};
+
+struct KernelArgs {
+  const uint16_t *q;  // fp16 bits
+  const int32_t *bt;
+  const int32_t *ctx;
+  float *out;
+  // balanced-schedule workspace
+  float *ws_ml;   // [slots][kMaxHeads][2]  (max in base-2 units, sum)
+  float *ws_acc;  // [slots][kMaxHeads][head_dim]
+  int *ws_count;  // [units]  merge counters, zero between calls
+  int *ws_info;   // [units][2]  {first worker, number of workers} (combine kernel mode)
+  // fixed-split partial arrays: [batch][splits][query_heads]([head_dim])
+  float *p_max;
+  float *p_sum;
+  float *p_out;
+  unsigned *err;  // device error word
+  int batch, qh, kvh, hd, ps, ps_shift, maxp, num_pages;
+  int g;        // query heads per K/V head
+  int sub;      // units per K/V head
+  int nh_unit;  // heads per unit (ceil(g / sub))
+  int ups;      // units per sequence = kvh * sub
+  float scale_log2;  // scale * log2(e)
+  int mode;
+  int num_splits;  // MODE_SPLIT
+  int workers;     // MODE_BALANCED: number of workers
+  int fused;       // MODE_BALANCED: last worker merges
+  int stages;
+  int warp_smem;   // bytes of dynamic shared memory per warp (multiple of kSmemAlign)
+};
+
+// ---- schedule arithmetic shared by the kernels and the host-side checks -------------
+
+PA_HD int tiles_of(int ctx, int tile_tokens) { return (ctx + tile_tokens - 1) / tile_tokens; }
+
+// Balanced schedule: worker c owns global tiles [start(c), start(c+1)) with
+// start(c) = floor(c * total / workers), where workers <= total (the kernel uses
+// min(launched workers, total)), so every range holds at least one tile and the workers
+// that share a unit are consecutive.
+PA_HD int64_t worker_start(int64_t c, int64_t total, int64_t workers) {
+  return (c * total) / workers;
+}
+
+// The worker whose range holds global tile x (0 <= x < total): the largest c with
+// start(c) <= x, i.e. floor(((x + 1) * workers - 1) / total).
+PA_HD int64_t worker_of(int64_t x, int64_t total, int64_t workers) {
+  return ((x + 1) * workers - 1) / total;
+}
+
+// Partial-state slot of (unit u, worker c): along the monotone path of (unit, worker)
+// pairs in tile order each step raises u or c, so u + c is unique; slots < units + workers.
+PA_HD int64_t slot_of(int64_t unit, int64_t worker) { return unit + worker; }
+
+// ---- launchers (defined in the .cu files) --------------------------------------------
+
+int tile_tokens(int head_dim, int mma);
+// Dynamic shared memory one worker warp needs (multiple of kSmemAlign).
+int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages);
+// SIMT kernels are instantiated for these head counts per unit; returns the smallest
+// instantiation >= nh.
+int simt_heads_instance(int nh);
+
+cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                          int mma, int nh_inst, int ctas, int warps_per_cta, size_t smem,
+                          cudaStream_t stream);
+cudaError_t launch_combine_balanced(const KernelArgs &a, int units, cudaStream_t stream);
+cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
+cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
+unsigned *device_error_word();
+
+}  // namespace pa
