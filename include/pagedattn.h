@@ -168,6 +168,32 @@ pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const v
                          const pa_options_t *options, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* Size of the fixed device scratch that pa_decode_noalloc uses (16 MiB). */
+#define PA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* pa_decode for callers that must not allocate device memory -- no counterpart in the
+ * paper; it exists for deployments, not for the method. A serving engine typically
+ * reserves nearly all of HBM for its K/V page pool at start-up and allows no allocation
+ * afterwards, and cudaMalloc/cudaFree synchronise the device, which a decode loop cannot
+ * afford; code running inside such an engine may have no allocator at all. This call
+ * never calls cudaMalloc, cudaFree or any allocating routine: when the heuristic's plan
+ * needs split-K scratch, it uses a 16 MiB array compiled into the library
+ * (PA_NOALLOC_SCRATCH_BYTES), which every GPU that loads the library holds until the
+ * process exits. Arguments, layouts and results are those of pa_decode; the caller still
+ * passes all inputs and the output.
+ *  - A plan that needs more scratch than PA_NOALLOC_SCRATCH_BYTES (pa_plan reports it in
+ *    workspace_bytes) is refused with PA_ERR_WORKSPACE before any launch.
+ *  - The first call on each device looks up the array's device address (and may load the
+ *    library's GPU code); make that first call before any stream capture begins.
+ *  - Every call shares the one array per device and it keeps the previous call's contents;
+ *    the merge counters in it are cleared on `stream` at the start of each call. Calls
+ *    whose work overlaps on the GPU (other streams, other host threads) race on the array
+ *    and give wrong results: serialise them. */
+pa_status_t pa_decode_noalloc(const pa_problem_t *problem, const void *query,
+                              const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables, const int32_t *context_lengths,
+                              float scale, float *out, void *stream);
+
 /* Split-K partial phase with a fixed number of splits per sequence, as in "[TIL]
  * Optimizing paged attention", section "V4 (Context-axis parallelism)": sequence b's
  * pages are cut into num_splits ranges of ceil(pages_b / num_splits) pages (the last

@@ -294,15 +294,25 @@ void fill_args(KernelArgs *a, const pa_problem_t *p, const Resolved &r, const vo
   a->err = device_error_word();
 }
 
-pa_status_t run(const pa_problem_t *p, const void *q, const void *k, const void *v,
-                const int32_t *bt, const int32_t *ctx, float scale, float *out,
-                const pa_options_t *o, void *ws, size_t ws_bytes, bool library_ws,
-                cudaStream_t stream) {
+}  // namespace
+
+namespace pa {
+
+pa_status_t validate_call(const pa_problem_t *p, const pa_options_t *o, const void *q,
+                          const void *k, const void *v, const int32_t *bt, const int32_t *ctx,
+                          float scale, const float *out) {
   pa_status_t st = check_problem(p);
   if (st != PA_OK) return st;
   st = check_options(o);
   if (st != PA_OK) return st;
-  st = check_tensors(q, k, v, bt, ctx, scale, out);
+  return check_tensors(q, k, v, bt, ctx, scale, out);
+}
+
+pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, const void *v,
+                        const int32_t *bt, const int32_t *ctx, float scale, float *out,
+                        const pa_options_t *o, void *ws, size_t ws_bytes, WorkspaceKind kind,
+                        cudaStream_t stream) {
+  pa_status_t st = validate_call(p, o, q, k, v, bt, ctx, scale, out);
   if (st != PA_OK) return st;
   if (p->batch == 0) return PA_OK;
   int dev = 0;
@@ -315,7 +325,7 @@ pa_status_t run(const pa_problem_t *p, const void *q, const void *k, const void 
   const pa_plan_t &pl = r.plan;
 
   if (pl.workspace_bytes > 0) {
-    if (library_ws) {
+    if (kind == WorkspaceKind::kLibrary) {
       st = library_workspace(dev, static_cast<size_t>(pl.workspace_bytes), stream, &ws);
       if (st != PA_OK) return st;
     } else if (!ws || ws_bytes < static_cast<size_t>(pl.workspace_bytes)) {
@@ -352,8 +362,13 @@ pa_status_t run(const pa_problem_t *p, const void *q, const void *k, const void 
     a.ws_acc = reinterpret_cast<float *>(base);
   }
   if (a.mode == MODE_BALANCED && a.fused) {
-    st = prepare_counters(ws, pl.units, stream);
-    if (st != PA_OK) return st;
+    if (kind == WorkspaceKind::kZeroEachCall) {
+      if (cudaMemsetAsync(ws, 0, static_cast<size_t>(pl.units) * 4, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    } else {
+      st = prepare_counters(ws, pl.units, stream);
+      if (st != PA_OK) return st;
+    }
   }
   if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, pl.ctas, pl.warps_per_cta,
                     static_cast<size_t>(pl.smem_bytes), stream) != cudaSuccess)
@@ -364,7 +379,9 @@ pa_status_t run(const pa_problem_t *p, const void *q, const void *k, const void 
   return PA_OK;
 }
 
-}  // namespace
+}  // namespace pa
+
+using namespace pa;
 
 extern "C" {
 
@@ -405,8 +422,9 @@ pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *str
 pa_status_t pa_decode(const pa_problem_t *problem, const void *query, const void *key_cache,
                       const void *value_cache, const int32_t *block_tables,
                       const int32_t *context_lengths, float scale, float *out, void *stream) {
-  return run(problem, query, key_cache, value_cache, block_tables, context_lengths, scale, out,
-             nullptr, nullptr, 0, true, static_cast<cudaStream_t>(stream));
+  return decode_into(problem, query, key_cache, value_cache, block_tables, context_lengths, scale,
+                     out, nullptr, nullptr, 0, WorkspaceKind::kLibrary,
+                     static_cast<cudaStream_t>(stream));
 }
 
 pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const void *key_cache,
@@ -414,8 +432,9 @@ pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const v
                          const int32_t *context_lengths, float scale, float *out,
                          const pa_options_t *options, void *workspace, size_t workspace_bytes,
                          void *stream) {
-  return run(problem, query, key_cache, value_cache, block_tables, context_lengths, scale, out,
-             options, workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
+  return decode_into(problem, query, key_cache, value_cache, block_tables, context_lengths, scale,
+                     out, options, workspace, workspace_bytes, WorkspaceKind::kCaller,
+                     static_cast<cudaStream_t>(stream));
 }
 
 pa_status_t pa_split_kv_partial(const pa_problem_t *problem, const void *query,

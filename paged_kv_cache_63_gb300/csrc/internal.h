@@ -95,3 +95,27 @@ cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
 unsigned *device_error_word();
 
 }  // namespace pa
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Who owns a decode call's workspace and how its merge counters are brought to zero.
+enum class WorkspaceKind {
+  kLibrary,      // library-owned grow-only buffer (pa_decode)
+  kCaller,       // caller buffer zeroed once by pa_workspace_init (pa_decode_ex)
+  kZeroEachCall  // fixed buffer whose counters are cleared on the stream before every call
+};
+
+// Host-side argument checks shared by the entry points (no GPU access).
+pa_status_t validate_call(const pa_problem_t *p, const pa_options_t *o, const void *q,
+                          const void *k, const void *v, const int32_t *bt, const int32_t *ctx,
+                          float scale, const float *out);
+
+// One decode step: validation, plan, workspace checks, tensor maps and launches.
+pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, const void *v,
+                        const int32_t *bt, const int32_t *ctx, float scale, float *out,
+                        const pa_options_t *o, void *ws, size_t ws_bytes, WorkspaceKind kind,
+                        cudaStream_t stream);
+
+}  // namespace pa

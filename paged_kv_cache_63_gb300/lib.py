@@ -29,6 +29,7 @@ COMBINE = {"fused": 0, "kernel": 1}
 
 # Every entry point include/pagedattn.h declares.
 EXPORTS = ("pa_plan", "pa_workspace_size", "pa_workspace_init", "pa_decode", "pa_decode_ex",
+           "pa_decode_noalloc",
            "pa_split_kv_partial", "pa_split_kv_combine", "pa_get_device_error",
            "pa_status_string", "pa_version")
 
@@ -86,6 +87,7 @@ def load(path: Optional[str] = None):
         lib.pa_decode.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, vp]
         lib.pa_decode_ex.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, P(pa_options_t),
                                      vp, ctypes.c_size_t, vp]
+        lib.pa_decode_noalloc.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, vp]
         lib.pa_split_kv_partial.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, i32, i32, vp,
                                             vp, vp, vp]
         lib.pa_split_kv_combine.argtypes = [P(pa_problem_t), i32, vp, vp, vp, vp, vp]
@@ -187,6 +189,18 @@ def pa_decode_ex(prob, query, key_cache, value_cache, block_tables, context_leng
                                float(scale), _ptr(out), ctypes.byref(opts) if opts else None,
                                _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "pa_decode_ex")
+
+
+def pa_decode_noalloc(prob, query, key_cache, value_cache, block_tables, context_lengths, scale,
+                      out, stream=None):
+    """pa_decode without any device allocation: split-K scratch comes from a fixed 16 MiB
+    array inside the library (for callers that may not allocate; see the header)."""
+    _check(load().pa_decode_noalloc(ctypes.byref(prob), _ptr(query), _ptr(key_cache),
+                                    _ptr(value_cache), _ptr(block_tables), _ptr(context_lengths),
+                                    float(scale), _ptr(out), _stream(stream)), "pa_decode_noalloc")
+
+
+PA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 def pa_split_kv_partial(prob, query, key_cache, value_cache, block_tables, context_lengths, scale,
