@@ -51,7 +51,7 @@ def parse_args():
                     help="CPU work for the oracle baseline sample")
     ap.add_argument("--math", default="auto")
     ap.add_argument("--schedule", default="auto")
-    ap.add_argument("--combine", default="fused")
+    ap.add_argument("--combine", default="auto")
     ap.add_argument("--workers", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--warps", type=int, default=0)
@@ -303,7 +303,7 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9
     kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
-    launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 1) else 1
+    launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 2) else 1
     traffic = recorded_traffic(w.name)
     line = {
         "metric": METRIC,

@@ -54,7 +54,7 @@ pa_status_t check_options(const pa_options_t *o) {
   if (!o) return PA_OK;
   if (o->schedule < PA_SCHEDULE_AUTO || o->schedule > PA_SCHEDULE_BALANCED) return PA_ERR_INVALID_ARG;
   if (o->math < PA_MATH_AUTO || o->math > PA_MATH_MMA) return PA_ERR_INVALID_ARG;
-  if (o->combine < PA_COMBINE_FUSED || o->combine > PA_COMBINE_KERNEL) return PA_ERR_INVALID_ARG;
+  if (o->combine < PA_COMBINE_AUTO || o->combine > PA_COMBINE_KERNEL) return PA_ERR_INVALID_ARG;
   if (o->workers < 0 || o->stages < 0 || o->stages > kMaxStages || o->warps_per_cta < 0 ||
       o->warps_per_cta > kMaxWarpsPerCta || o->reserved[0] || o->reserved[1])
     return PA_ERR_INVALID_ARG;
@@ -135,7 +135,9 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
   pl.tile_tokens = tile_tokens(p->head_dim, r->mma);
 
   const int stage_bytes = pl.tile_tokens * p->head_dim * 4;
-  int stages = (o && o->stages) ? o->stages : (stage_bytes >= 16384 ? 3 : 4);
+  // Two 16 KB stages per warp already keep ~64 KB per SM in flight, which saturates HBM
+  // for this scattered access pattern; deeper rings only add queueing (measured on GB300).
+  int stages = (o && o->stages) ? o->stages : (stage_bytes >= 16384 ? 2 : 4);
   int per_warp = warp_smem_bytes(p->head_dim, r->mma, r->nh_inst, stages);
   int warps = (o && o->warps_per_cta) ? o->warps_per_cta
                                       : std::min(kMaxWarpsPerCta,
@@ -164,7 +166,17 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
     pl.workspace_bytes = 0;
   } else {
     pl.workers = (o && o->workers) ? o->workers : capacity;
-    pl.combine = o ? o->combine : PA_COMBINE_FUSED;
+    pl.combine = o ? o->combine : PA_COMBINE_AUTO;
+    if (pl.combine == PA_COMBINE_AUTO) {
+      // With more units than workers most units are whole in one worker and the few shared
+      // ones are merged by their last worker at no cost; with more workers than units most
+      // units are shared, and a separate combine kernel (a CTA per (unit, head), launched
+      // as a programmatic dependent) keeps one warp from reading every partial state at
+      // the end.
+      pl.combine = static_cast<int64_t>(pl.workers) >= static_cast<int64_t>(units)
+                       ? PA_COMBINE_KERNEL
+                       : PA_COMBINE_FUSED;
+    }
     const int64_t slots = static_cast<int64_t>(units) + pl.workers;
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
     pl.workspace_bytes = al(int64_t(units) * 4) + al(int64_t(units) * 8) +
@@ -226,16 +238,20 @@ void note_zeroed(const void *ws, size_t bytes) {
   g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = static_cast<int64_t>(bytes / 4);
 }
 
-pa_status_t prepare_counters(void *ws, int64_t units, cudaStream_t stream) {
+// `fused`: this call merges through the counters, so the first `units` must be zero.
+// Either way the call writes partial states past its own counter region, so afterwards at
+// most `units` leading counters are known to be zero.
+pa_status_t prepare_counters(void *ws, int64_t units, bool fused, cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_zero_mu);
   auto it = g_zero_counters.find(reinterpret_cast<uintptr_t>(ws));
-  const int64_t known = it == g_zero_counters.end() ? 0 : it->second;
-  if (units > known) {
+  int64_t known = it == g_zero_counters.end() ? 0 : it->second;
+  if (fused && units > known) {
     if (cudaMemsetAsync(static_cast<char *>(ws) + known * 4, 0,
                         static_cast<size_t>(units - known) * 4, stream) != cudaSuccess)
       return PA_ERR_CUDA;
+    known = units;
   }
-  g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = units;
+  g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = std::min(known, units);
   return PA_OK;
 }
 
@@ -361,12 +377,13 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
     base += al(slots * kMaxHeads * 2 * 4);
     a.ws_acc = reinterpret_cast<float *>(base);
   }
-  if (a.mode == MODE_BALANCED && a.fused) {
+  if (a.mode == MODE_BALANCED) {
     if (kind == WorkspaceKind::kZeroEachCall) {
-      if (cudaMemsetAsync(ws, 0, static_cast<size_t>(pl.units) * 4, stream) != cudaSuccess)
+      if (a.fused &&
+          cudaMemsetAsync(ws, 0, static_cast<size_t>(pl.units) * 4, stream) != cudaSuccess)
         return PA_ERR_CUDA;
     } else {
-      st = prepare_counters(ws, pl.units, stream);
+      st = prepare_counters(ws, pl.units, a.fused != 0, stream);
       if (st != PA_OK) return st;
     }
   }
@@ -374,7 +391,7 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
                     static_cast<size_t>(pl.smem_bytes), stream) != cudaSuccess)
     return PA_ERR_CUDA;
   if (a.mode == MODE_BALANCED && !a.fused) {
-    if (launch_combine_balanced(a, pl.units, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_combine_balanced(a, pl.units, r.nh_unit, stream) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
 }

@@ -104,40 +104,50 @@ __device__ __forceinline__ void advance(const KernelArgs &a, Cursor &c, int T) {
 __device__ inline bool balanced_start(const KernelArgs &a, int worker, int T, Cursor &c,
                                       long long &total, long long &nworkers) {
   const int lane = threadIdx.x & 31;
-  long long tiles = 0;
-  for (int base = 0; base < a.batch; base += 32) {
-    const int b = base + lane;
-    const int t = b < a.batch ? tiles_of(load_ctx(a, b), T) : 0;
-    tiles += warp_sum(static_cast<long long>(t));
+  // lane l owns the contiguous sequences [b0, b1); its loads are independent of each
+  // other, so the whole scan costs about one memory round trip
+  const int blk = (a.batch + 31) >> 5;
+  const int b0 = min(lane * blk, a.batch);
+  const int b1 = min(b0 + blk, a.batch);
+  long long mine = 0;
+#pragma unroll 16
+  for (int b = b0; b < b1; ++b) mine += tiles_of(load_ctx(a, b), T);
+  long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  total = tiles * a.ups;
+  total = __shfl_sync(0xffffffffu, incl, 31) * a.ups;
   nworkers = total < a.workers ? total : a.workers;
   if (worker >= nworkers) return false;
   const long long s = worker_start(worker, total, nworkers);
   const long long e = worker_start(worker + 1, total, nworkers);
-  long long run = 0;
-  for (int base = 0; base < a.batch; base += 32) {
+  // the lane whose block holds global tile s, then that block walked 32 sequences at a time
+  const int L = __ffs(__ballot_sync(0xffffffffu, incl * a.ups > s)) - 1;
+  long long run = __shfl_sync(0xffffffffu, incl - mine, L) * a.ups;
+  const int lb0 = min(L * blk, a.batch);
+  const int lb1 = min(lb0 + blk, a.batch);
+  for (int base = lb0; base < lb1; base += 32) {
     const int b = base + lane;
-    const long long t =
-        b < a.batch ? static_cast<long long>(tiles_of(load_ctx(a, b), T)) * a.ups : 0;
-    long long incl = t;
+    const long long t = b < lb1 ? static_cast<long long>(tiles_of(load_ctx(a, b), T)) * a.ups : 0;
+    long long in2 = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
+      const long long y = __shfl_up_sync(0xffffffffu, in2, o);
+      if (lane >= o) in2 += y;
     }
-    const long long chunk = __shfl_sync(0xffffffffu, incl, 31);
+    const long long chunk = __shfl_sync(0xffffffffu, in2, 31);
     if (s < run + chunk) {
-      const unsigned m = __ballot_sync(0xffffffffu, run + incl > s);
-      const int L = __ffs(m) - 1;
-      const long long excl = __shfl_sync(0xffffffffu, incl - t, L);
-      c.b = base + L;
+      const int M = __ffs(__ballot_sync(0xffffffffu, run + in2 > s)) - 1;
+      const long long excl = run + __shfl_sync(0xffffffffu, in2 - t, M);
+      c.b = base + M;
       c.end = load_ctx(a, c.b);
       const int tb = tiles_of(c.end, T);
-      const long long inner = s - (run + excl);
+      const long long inner = s - excl;
       c.us = static_cast<int>(inner / tb);
       c.tok = static_cast<int>(inner % tb) * T;
-      c.ug0 = run + excl + static_cast<long long>(c.us) * tb;
+      c.ug0 = excl + static_cast<long long>(c.us) * tb;
       c.left = static_cast<int>(e - s);
       return true;
     }
@@ -398,7 +408,8 @@ __device__ __forceinline__ void simt_tile(SimtState<HD, NH> &st, uint32_t stk, u
 // ------------------------------------------------------------------ MMA arithmetic
 template <int HD>
 struct MmaState {
-  float m, lsum;          // row (head) lane / 4
+  float m, lsum;          // row (head) lane / 4: reference maximum and sum relative to it
+  float mx;               // the row's true running maximum (m <= mx <= m + kRescaleSlack)
   float o[HD / 8][2];     // O[lane / 4][8 nt + 2 (lane % 4) + {0, 1}]
   uint32_t qa[HD / 16][2];  // A fragments of q: rows 0..7, k = 16 ks + 2 (lane % 4) (+8)
 };
@@ -417,6 +428,7 @@ __device__ __forceinline__ void mma_begin(MmaState<HD> &st, const KernelArgs &a,
     st.qa[ks][1] = h < nh ? __ldg(src + (ks * 16 + 8 + c) / 2) : 0u;
   }
   st.m = -INFINITY;
+  st.mx = -INFINITY;
   st.lsum = 0.f;
 #pragma unroll
   for (int nt = 0; nt < HD / 8; ++nt) st.o[nt][0] = st.o[nt][1] = 0.f;
@@ -435,32 +447,59 @@ __device__ __forceinline__ void zero_v_rows(uint32_t stv, int from) {
   }
 }
 
+// Per-lane ldmatrix addresses inside a stage, fixed for the whole kernel. For K (score
+// phase) the lane supplies row (mi >> 1) * 8 + rr of a 16-token chunk and 16-byte chunk
+// 2 j + (mi & 1) of a 64-column block (j = ks & 3); for V (value phase) row
+// (mi & 1) * 8 + rr and chunk 2 j + (mi >> 1). Rows of a chunk are 8-aligned, so the
+// swizzle term is the lane's rr; the chunk's 64-column block and 16-token offset are
+// compile-time constants added at the use.
 template <int HD, int T>
-__device__ __forceinline__ void mma_tile(MmaState<HD> &st, uint32_t stk, int tok0, int end,
-                                         float scale_log2) {
+struct MmaLane {
+  uint32_t k[4], v[4];
+  __device__ __forceinline__ void init() {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3;
+    const int rr = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      k[j] = static_cast<uint32_t>(((mi >> 1) * 8 + rr) * 128 + (((2 * j + (mi & 1)) ^ rr) << 4));
+      v[j] = static_cast<uint32_t>(Geom<HD, T>::kHalfBytes + ((mi & 1) * 8 + rr) * 128 +
+                                   (((2 * j + (mi >> 1)) ^ rr) << 4));
+    }
+  }
+};
+
+// Rescale threshold of the online softmax, in base-2 units: the reference maximum of a row
+// moves only when a tile's maximum exceeds it by more than this, so the fp16 probabilities
+// stay <= 2^8 and most tiles skip rescaling the accumulators.
+constexpr float kRescaleSlack = 8.f;
+
+template <int HD, int T>
+__device__ __forceinline__ void mma_tile(MmaState<HD> &st, const MmaLane<HD, T> &ln,
+                                         uint32_t stage, int tok0, int end, float scale_log2) {
   constexpr int NCH = T / 16;
   const int lane = threadIdx.x & 31;
-  const int mi = lane >> 3;
-  const int rr = lane & 7;
-  const uint32_t stv = stk + Geom<HD, T>::kHalfBytes;
+  uint32_t kb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) kb[j] = stage + ln.k[j];
 
   // S[h][t] for the tile's 16-token chunks: two n8 tiles per chunk
   float sc[NCH][2][2];
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
     sc[ch][0][0] = sc[ch][0][1] = sc[ch][1][0] = sc[ch][1][1] = 0.f;
-    const int krow = ch * 16 + (mi >> 1) * 8 + rr;
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(stk + tile_off<HD, T>(krow, ks * 2 + (mi & 1)), b0, b1, b2, b3);
+      ldsm_x4(kb[ks & 3] + (ks >> 2) * (T * 128) + ch * 2048, b0, b1, b2, b3);
       mma_rows8(sc[ch][0][0], sc[ch][0][1], st.qa[ks][0], st.qa[ks][1], b0, b1);
       mma_rows8(sc[ch][1][0], sc[ch][1][1], st.qa[ks][0], st.qa[ks][1], b2, b3);
     }
   }
 
-  // online softmax (base 2) for row lane / 4: the row's 16 * NCH scores live in the 4
-  // lanes lane & ~3 .. lane | 3
+  // online softmax (base 2) for row lane / 4; the row's scores live in lanes
+  // lane & ~3 .. lane | 3. Tokens past `end` are masked only on a partial tile.
+  const bool partial = end - tok0 < T;
   float mt = -INFINITY;
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch)
@@ -468,46 +507,51 @@ __device__ __forceinline__ void mma_tile(MmaState<HD> &st, uint32_t stk, int tok
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int tok = tok0 + ch * 16 + nt * 8 + 2 * (lane & 3) + j;
-        const float x = tok < end ? sc[ch][nt][j] * scale_log2 : -INFINITY;
+        float x = sc[ch][nt][j] * scale_log2;
+        if (partial) {
+          const int tok = tok0 + ch * 16 + nt * 8 + 2 * (lane & 3) + j;
+          x = tok < end ? x : -INFINITY;
+        }
         sc[ch][nt][j] = x;
         mt = fmaxf(mt, x);
       }
   mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
   mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-  const float mn = fmaxf(st.m, mt);
-  const float alpha = fast_exp2(st.m - mn);
-  st.m = mn;
+  st.mx = fmaxf(st.mx, mt);
+  if (__any_sync(0xffffffffu, mt > st.m + kRescaleSlack)) {
+    const float mn = fmaxf(st.m, mt);
+    const float alpha = fast_exp2(st.m - mn);
+    st.m = mn;
+    st.lsum *= alpha;
+#pragma unroll
+    for (int nt = 0; nt < HD / 8; ++nt) {
+      st.o[nt][0] *= alpha;
+      st.o[nt][1] *= alpha;
+    }
+  }
   float psum = 0.f;
   uint32_t pa[NCH][2];
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float p0 = fast_exp2(sc[ch][nt][0] - mn);
-      const float p1 = fast_exp2(sc[ch][nt][1] - mn);
+      const float p0 = fast_exp2(sc[ch][nt][0] - st.m);
+      const float p1 = fast_exp2(sc[ch][nt][1] - st.m);
       psum += p0 + p1;
       pa[ch][nt] = pack_half2(p0, p1);
     }
-  st.lsum = st.lsum * alpha + psum;
-#pragma unroll
-  for (int nt = 0; nt < HD / 8; ++nt) {
-    st.o[nt][0] *= alpha;
-    st.o[nt][1] *= alpha;
-  }
+  st.lsum += psum;
 
-  const int nvalid = end - tok0;
-  if (nvalid < T) {
-    zero_v_rows<HD, T>(stv, nvalid);
+  if (partial) {
+    zero_v_rows<HD, T>(stage + Geom<HD, T>::kHalfBytes, end - tok0);
     __syncwarp();
   }
 #pragma unroll
   for (int ch = 0; ch < NCH; ++ch) {
-    const int vrow = ch * 16 + (mi & 1) * 8 + rr;
 #pragma unroll
     for (int dt = 0; dt < HD / 16; ++dt) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_trans(stv + tile_off<HD, T>(vrow, dt * 2 + (mi >> 1)), b0, b1, b2, b3);
+      ldsm_x4_trans(stage + ln.v[dt & 3] + (dt >> 2) * (T * 128) + ch * 2048, b0, b1, b2, b3);
       mma_rows8(st.o[2 * dt][0], st.o[2 * dt][1], pa[ch][0], pa[ch][1], b0, b1);
       mma_rows8(st.o[2 * dt + 1][0], st.o[2 * dt + 1][1], pa[ch][0], pa[ch][1], b2, b3);
     }
@@ -515,40 +559,75 @@ __device__ __forceinline__ void mma_tile(MmaState<HD> &st, uint32_t stk, int tok
 }
 
 // ------------------------------------------------------------------ merge (log-sum-exp)
-// Merge n partial states of one unit (balanced layout, slots unit + c0 .. unit + c0 + n - 1,
-// in that order) into normalised rows of `out`; lanes own head_dim / 32 dims.
+// Merge the n partial states of one unit (balanced layout: slots unit + c0 .. unit + c0 +
+// n - 1) into normalised rows of `out`, all heads at once, by one warp. Two passes instead
+// of the sequential online merge, so that loads do not wait on each other: the common
+// maximum M_h per head first, then out_h = sum_k 2^(m_hk - M_h) acc_hk / sum_k 2^(m_hk - M_h)
+// l_hk, summed in contributor order (states with l = 0 are empty and skipped). Lanes own
+// head_dim / 32 dims.
 template <int HD>
 __device__ __forceinline__ void merge_balanced(const KernelArgs &a, long long unit, long long c0,
                                                int n, int b, int h0, int nh) {
   constexpr int DPL = HD / 32;
   const int lane = threadIdx.x & 31;
-  for (int h = 0; h < nh; ++h) {
-    float M = -INFINITY, L = 0.f;
-    float O[DPL];
+  const int hl = lane >> 2;  // pass 1: lane (hl, lane & 3) scans contributors k = lane & 3 (mod 4)
+  float mx = -INFINITY;
+  if (hl < nh) {
+    for (int k = lane & 3; k < n; k += 4) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+          a.ws_ml + (slot_of(unit, c0 + k) * kMaxHeads + hl) * 2));
+      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+    }
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  float M[kMaxHeads];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) O[i] = 0.f;
+  for (int h = 0; h < kMaxHeads; ++h) M[h] = __shfl_sync(0xffffffffu, mx, 4 * h);
+
+  // heads in groups of HG so the accumulators stay in registers
+  constexpr int HG = HD >= 256 ? 4 : kMaxHeads;
+#pragma unroll
+  for (int g0 = 0; g0 < kMaxHeads; g0 += HG) {
+    if (g0 >= nh) break;
+    float O[HG][DPL];
+    float L[HG];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      L[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) O[h][i] = 0.f;
+    }
+#pragma unroll(HD >= 256 ? 1 : 2)
     for (int k = 0; k < n; ++k) {
       const long long slot = slot_of(unit, c0 + k);
-      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
-      if (ml.y == 0.f) continue;
-      const float Mn = fmaxf(M, ml.x);
-      const float al = fast_exp2(M - Mn);
-      const float be = fast_exp2(ml.x - Mn);
-      L = al * L + be * ml.y;
-      const float *src = a.ws_acc + (slot * kMaxHeads + h) * HD + lane * DPL;
+      const float *ml = a.ws_ml + (slot * kMaxHeads + g0) * 2;
+      const float *acc = a.ws_acc + (slot * kMaxHeads + g0) * HD + lane * DPL;
 #pragma unroll
-      for (int i = 0; i < DPL; i += 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
-        O[i] = al * O[i] + be * v.x;
-        O[i + 1] = al * O[i + 1] + be * v.y;
+      for (int h = 0; h < HG; ++h) {
+        if (g0 + h < nh) {
+          const float2 s = __ldcg(reinterpret_cast<const float2 *>(ml + 2 * h));
+          const float w = s.y > 0.f ? fast_exp2(s.x - M[g0 + h]) : 0.f;
+          L[h] += w * s.y;
+#pragma unroll
+          for (int i = 0; i < DPL; i += 2) {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(acc + h * HD + i));
+            O[h][i] += w * v.x;
+            O[h][i + 1] += w * v.y;
+          }
+        }
       }
-      M = Mn;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    float *dst = a.out + (static_cast<long long>(b) * a.qh + h0 + h) * HD + lane * DPL;
 #pragma unroll
-    for (int i = 0; i < DPL; i += 2)
-      *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
+    for (int h = 0; h < HG; ++h) {
+      if (g0 + h < nh) {
+        const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
+        float *dst = a.out + (static_cast<long long>(b) * a.qh + h0 + g0 + h) * HD + lane * DPL;
+#pragma unroll
+        for (int i = 0; i < DPL; i += 2)
+          *reinterpret_cast<float2 *>(dst + i) = make_float2(O[h][i] * inv, O[h][i + 1] * inv);
+      }
+    }
   }
 }
 
@@ -590,6 +669,8 @@ struct Epilogue<HD, true, NH> {
       *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(st.o[nt][0] * inv, st.o[nt][1] * inv);
   }
   // Partial state to (max, sum, acc) arrays with per-head strides.
+  // Partial state relative to the row's true maximum (the running sum and accumulator are
+  // kept against a reference maximum up to kRescaleSlack lower; rebased here).
   template <typename St>
   __device__ static void partial_out(St &st, const UnitInfo &u, float *mx, float *sm, float *acc,
                                      long long head_stride_ml, long long head_stride_acc) {
@@ -599,14 +680,16 @@ struct Epilogue<HD, true, NH> {
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     const int h = lane >> 2;
     if (h >= u.nh) return;
+    const float rebase = fast_exp2(st.m - st.mx);
     if ((lane & 3) == 0) {
-      mx[h * head_stride_ml] = st.m;
-      sm[h * head_stride_ml] = l;
+      mx[h * head_stride_ml] = st.mx;
+      sm[h * head_stride_ml] = l * rebase;
     }
     float *dst = acc + h * head_stride_acc + 2 * (lane & 3);
 #pragma unroll
     for (int nt = 0; nt < HD / 8; ++nt)
-      *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(st.o[nt][0], st.o[nt][1]);
+      *reinterpret_cast<float2 *>(dst + nt * 8) =
+          make_float2(st.o[nt][0] * rebase, st.o[nt][1] * rebase);
   }
 };
 
@@ -649,6 +732,19 @@ struct Epilogue<HD, false, NH> {
   }
 };
 
+// Warm L2 with the query rows of the unit at cursor c (used when the consuming cursor
+// reaches that unit a few tiles later).
+template <int HD>
+__device__ __forceinline__ void prefetch_q(const KernelArgs &a, const Cursor &c) {
+  const int lane = threadIdx.x & 31;
+  const UnitInfo u = unit_info(a, c.b, c.us);
+  const int lines = u.nh * HD * 2 / 128;
+  if (lane < lines) {
+    const uint16_t *p = a.q + (static_cast<long long>(c.b) * a.qh + u.h0) * HD + lane * 64;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+  }
+}
+
 // Zero the output rows of a unit (a context of length 0).
 template <int HD>
 __device__ __forceinline__ void zero_unit(const KernelArgs &a, const UnitInfo &u) {
@@ -676,6 +772,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   const uint32_t pbuf = qs + NH * HD * 4;           // SIMT: probabilities [T][NHP]
   const uint32_t bar0 = smem_addr(&bars[warp * kMaxStages]);
 
+  // a combine kernel launched as this grid's programmatic dependent may start now; it
+  // waits for this grid's completion before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---- the worker's range
   Cursor c;
   long long total = 0, nworkers = 0;
@@ -683,14 +783,21 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   if (a.mode == MODE_BALANCED) {
     if (worker >= a.workers) return;
     const bool any = balanced_start(a, worker, T, c, total, nworkers);
-    // sequences with an empty context: zero their rows (worker b mod workers)
-    for (int b = worker; b < a.batch; b += a.workers) {
-      if (load_ctx(a, b) != 0) continue;
-      for (int us = 0; us < a.ups; ++us) {
-        zero_unit<HD>(a, unit_info(a, b, us));
-        if (!a.fused && lane == 0) {
-          a.ws_info[2 * (b * a.ups + us)] = 0;
-          a.ws_info[2 * (b * a.ups + us) + 1] = 0;
+    // sequences with an empty context: zero their rows (worker b mod workers); lanes test
+    // 32 candidate sequences at once
+    for (long long base = worker; base < a.batch; base += 32ll * a.workers) {
+      const long long bl = base + static_cast<long long>(lane) * a.workers;
+      unsigned empty = __ballot_sync(0xffffffffu, bl < a.batch && load_ctx(a, static_cast<int>(bl)) == 0);
+      while (empty) {
+        const int j = __ffs(empty) - 1;
+        empty &= empty - 1;
+        const int b = static_cast<int>(base + static_cast<long long>(j) * a.workers);
+        for (int us = 0; us < a.ups; ++us) {
+          zero_unit<HD>(a, unit_info(a, b, us));
+          if (!a.fused && lane == 0) {
+            a.ws_info[2 * (b * a.ups + us)] = 0;
+            a.ws_info[2 * (b * a.ups + us) + 1] = 0;
+          }
         }
       }
     }
@@ -759,6 +866,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   }
 
   typename std::conditional<MMA, MmaState<HD>, SimtState<HD, NH>>::type st;
+  MmaLane<HD, T> lane_addr;
+  if constexpr (MMA) lane_addr.init();
   UnitInfo cur;
   cur.b = -1;
   cur.us = -1;
@@ -823,7 +932,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
       const int s = issued % S;
       issue_tile<HD, T>(a, &tk, &tv, ic, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol);
       ++issued;
+      const int ib = ic.b, ius = ic.us;
       advance(a, ic, T);
+      if (ic.left > 0 && (ic.b != ib || ic.us != ius)) prefetch_q<HD>(a, ic);
     }
     const int s = consumed % S;
     if (!mbar_wait(bar0 + 8 * s, static_cast<uint32_t>((consumed / S) & 1), a.err)) {
@@ -832,7 +943,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     }
     const uint32_t stk = wbase + s * G::kStageBytes;
     if constexpr (MMA)
-      mma_tile<HD, T>(st, stk, c.tok, c.end, a.scale_log2);
+      mma_tile<HD, T>(st, lane_addr, stk, c.tok, c.end, a.scale_log2);
     else
       simt_tile<HD, T, NH>(st, stk, qs, pbuf, c.tok, c.end);
     fence_proxy_async();
@@ -849,16 +960,75 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   finish_unit();
 }
 
-// Separate log-sum-exp combine for the balanced schedule: one warp per unit.
+// Separate log-sum-exp combine for the balanced schedule: one CTA of 8 warps per (unit,
+// head), for units shared by many workers. It is launched as a programmatic dependent of
+// the decode kernel, so its CTAs are resident before the decode finishes and start the
+// moment the decode's writes are visible (griddepcontrol.wait). Two passes as in
+// merge_balanced: the maximum over contributors, then the weighted sums; warp w takes
+// contributors w, w + 8, ... and the 8 partial sums are added in warp order.
 template <int HD>
-__global__ void __launch_bounds__(256) combine_balanced_kernel(const __grid_constant__ KernelArgs a) {
-  const long long unit = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (unit >= static_cast<long long>(a.batch) * a.ups) return;
+__global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant__ KernelArgs a) {
+  constexpr int DPL = HD / 32;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long unit = blockIdx.x;
+  const int h = blockIdx.y;
   const int c0 = a.ws_info[2 * unit];
   const int n = a.ws_info[2 * unit + 1];
   if (n <= 1) return;
   const UnitInfo u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
-  merge_balanced<HD>(a, unit, c0, n, u.b, u.h0, u.nh);
+  if (h >= u.nh) return;
+  __shared__ float s_max[8];
+  __shared__ float s_l[8];
+  __shared__ __align__(16) float s_acc[8][HD];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  float mx = -INFINITY;
+  for (int k = tid; k < n; k += 256) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+        a.ws_ml + (slot_of(unit, c0 + k) * kMaxHeads + h) * 2));
+    if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) s_max[warp] = mx;
+  __syncthreads();
+  float M = s_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_max[w]);
+  float O[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) O[i] = 0.f;
+  float L = 0.f;
+#pragma unroll 2
+  for (int k = warp; k < n; k += 8) {
+    const long long slot = slot_of(unit, c0 + k);
+    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
+    const float w = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+    L += w * ml.y;
+    const float *src = a.ws_acc + (slot * kMaxHeads + h) * HD + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2) {
+      const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
+      O[i] += w * v.x;
+      O[i + 1] += w * v.y;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) s_acc[warp][lane * DPL + i] = O[i];
+  if (lane == 0) s_l[warp] = L;
+  __syncthreads();
+  float Lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) Lt += s_l[w];
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+  float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0 + h) * HD;
+  for (int d = tid; d < HD; d += 256) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) o += s_acc[w][d];
+    dst[d] = o * inv;
+  }
 }
 
 // Log-sum-exp combine of the fixed-split arrays: one warp per (sequence, query head).

@@ -47,12 +47,20 @@ cudaError_t launch_decode_hd(const KernelArgs &a, const CUtensorMap *tk, const C
 }
 
 template <int HD>
-cudaError_t launch_combine_balanced_hd(const KernelArgs &a, int units, cudaStream_t stream) {
-  const long long threads = static_cast<long long>(units) * 32;
-  const int blocks = static_cast<int>((threads + 255) / 256);
-  if (blocks == 0) return cudaSuccess;
-  combine_balanced_kernel<HD><<<blocks, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_combine_balanced_hd(const KernelArgs &a, int units, int heads,
+                                       cudaStream_t stream) {
+  if (units == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units), static_cast<unsigned>(heads), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_wide_kernel<HD>, a);
 }
 
 template <int HD>
@@ -73,9 +81,9 @@ cudaError_t launch_combine_split_hd(const KernelArgs &a, cudaStream_t stream) {
                                    int warps, size_t smem, cudaStream_t stream) {            \
     return launch_decode_hd<HD>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);         \
   }                                                                                          \
-  cudaError_t launch_combine_balanced_hd##HD(const KernelArgs &a, int units,                 \
+  cudaError_t launch_combine_balanced_hd##HD(const KernelArgs &a, int units, int heads,      \
                                              cudaStream_t stream) {                          \
-    return launch_combine_balanced_hd<HD>(a, units, stream);                                 \
+    return launch_combine_balanced_hd<HD>(a, units, heads, stream);                          \
   }                                                                                          \
   cudaError_t launch_combine_split_hd##HD(const KernelArgs &a, cudaStream_t stream) {        \
     return launch_combine_split_hd<HD>(a, stream);                                           \

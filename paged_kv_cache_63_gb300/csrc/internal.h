@@ -89,7 +89,8 @@ int simt_heads_instance(int nh);
 cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                           int mma, int nh_inst, int ctas, int warps_per_cta, size_t smem,
                           cudaStream_t stream);
-cudaError_t launch_combine_balanced(const KernelArgs &a, int units, cudaStream_t stream);
+cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads,
+                                    cudaStream_t stream);
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
 unsigned *device_error_word();

@@ -25,7 +25,7 @@ PA_DEVERR_CONTEXT = 2
 PA_DEVERR_TIMEOUT = 4
 SCHEDULE = {"auto": 0, "single": 1, "balanced": 2}
 MATH = {"auto": 0, "simt": 1, "mma": 2}
-COMBINE = {"fused": 0, "kernel": 1}
+COMBINE = {"auto": 0, "fused": 1, "kernel": 2}
 
 # Every entry point include/pagedattn.h declares.
 EXPORTS = ("pa_plan", "pa_workspace_size", "pa_workspace_init", "pa_decode", "pa_decode_ex",
@@ -116,7 +116,7 @@ def problem_of(w) -> pa_problem_t:
                    w.max_pages_per_sequence, w.num_physical_pages)
 
 
-def options(schedule="auto", math="auto", combine="fused", workers=0, stages=0,
+def options(schedule="auto", math="auto", combine="auto", workers=0, stages=0,
             warps_per_cta=0) -> pa_options_t:
     o = pa_options_t()
     o.schedule = SCHEDULE[schedule] if isinstance(schedule, str) else int(schedule)

@@ -102,7 +102,13 @@ def test_plan_heuristic():
     assert pl["schedule"] == 1 and pl["workspace_bytes"] == 0 and pl["workers"] == 4096 * 8
     # forced options are honoured
     pl = lib.pa_plan(P(), lib.options(schedule="balanced", workers=7, combine="kernel"))
-    assert (pl["schedule"], pl["workers"], pl["combine"]) == (2, 7, 1)
+    assert (pl["schedule"], pl["workers"], pl["combine"]) == (2, 7, 2)
+    # many workers per unit: the separate combine kernel; few: the fused merge
+    pl = lib.pa_plan(P(batch=4, query_heads=24, kv_heads=4, head_dim=256, page_size=64,
+                       max_pages_per_sequence=1563, num_physical_pages=6252))
+    assert pl["combine"] == 2
+    assert lib.pa_plan(P(batch=256, query_heads=64, kv_heads=8))["combine"] == 1
+    assert lib.pa_plan(P(batch=32, query_heads=32, kv_heads=8))["combine"] == 2
 
 
 def test_workspace_bytes_cover_slots():

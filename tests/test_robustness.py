@@ -140,13 +140,18 @@ def test_workspace_follows_shape_changes():
     import oracle
 
     t = torch()
+    # long_gqa6 has few units and takes the separate combine kernel, whose partial states
+    # land where a later fused call keeps its counters
     seq = [make_workload("gqa4_mid", batch=3), make_workload("ragged", batch=20),
+           make_workload("long_gqa6", context_lengths=[3000, 500]),
            make_workload("gqa4_mid", batch=5), make_workload("ragged", batch=30),
-           make_workload("tiny"), make_workload("ragged", batch=30)]
+           make_workload("tiny"), make_workload("long_gqa6", context_lengths=[900]),
+           make_workload("ragged", batch=30)]
     refs = [oracle.decode(w) for w in seq]
     for w, ref in zip(seq, refs):  # library-owned workspace (pa_decode)
         assert_close(run(w), ref, f"pa_decode {w.name} b={w.batch}")
     opts = lib.options(schedule="balanced")
+    assert {lib.pa_plan(lib.problem_of(w), opts)["combine"] for w in seq} == {1, 2}
     n = max(lib.pa_workspace_size(lib.problem_of(w), opts) for w in seq)
     ws = t.empty(n, dtype=t.uint8, device="cuda")
     lib.pa_workspace_init(ws, n)
