@@ -106,10 +106,12 @@ typedef struct pa_options_t {
   int32_t schedule;    /* pa_schedule_t */
   int32_t math;        /* pa_math_t */
   int32_t combine;     /* pa_combine_t */
-  int32_t workers;     /* balanced: number of workers (warps); 0 = as many as fit at once */
+  int32_t workers;     /* balanced: number of warps that take K/V tiles (rounded up to a
+                          multiple of the plan's group); 0 = as many as fit at once */
   int32_t stages;      /* K/V pipeline depth per worker; 0 = default */
   int32_t warps_per_cta; /* 0 = default */
-  int32_t reserved[2]; /* must be 0 */
+  int32_t tile_tokens; /* tokens per K/V tile: 0 = default; 16 or 32 for head_dim 128 */
+  int32_t reserved[1]; /* must be 0 */
 } pa_options_t;
 
 /* What pa_decode / pa_decode_ex will launch for a problem (filled by pa_plan). */
@@ -123,7 +125,9 @@ typedef struct pa_plan_t {
   int32_t stages;
   int32_t tile_tokens;    /* tokens per K/V tile */
   int32_t units;          /* batch * kv_heads * ceil(g / 8): (sequence, head group) units */
-  int32_t heads_per_unit; /* query heads one worker serves with one K/V read (<= 8) */
+  int32_t heads_per_unit; /* query heads one warp serves with one K/V read (<= 8) */
+  int32_t group;          /* warps per worker: they serve neighbouring units of a sequence
+                             over the same tokens */
   int64_t smem_bytes;     /* dynamic shared memory per CTA */
   int64_t workspace_bytes;/* bytes pa_decode_ex needs for this plan */
 } pa_plan_t;

@@ -22,6 +22,7 @@ constexpr int kMaxDev = 64;
 constexpr int kSmemReservedPerCta = 1024;
 // Static shared memory of the decode kernel (its mbarriers), rounded up.
 constexpr int kStaticSmem = 1024;
+constexpr int kDefaultWarps = 8;
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -56,7 +57,7 @@ pa_status_t check_options(const pa_options_t *o) {
   if (o->math < PA_MATH_AUTO || o->math > PA_MATH_MMA) return PA_ERR_INVALID_ARG;
   if (o->combine < PA_COMBINE_AUTO || o->combine > PA_COMBINE_KERNEL) return PA_ERR_INVALID_ARG;
   if (o->workers < 0 || o->stages < 0 || o->stages > kMaxStages || o->warps_per_cta < 0 ||
-      o->warps_per_cta > kMaxWarpsPerCta || o->reserved[0] || o->reserved[1])
+      o->warps_per_cta > kMaxWarpsPerCta || o->tile_tokens < 0 || o->reserved[0])
     return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
@@ -111,6 +112,15 @@ struct Resolved {
   int g, sub, nh_unit, nh_inst, mma, ctas_per_sm;
 };
 
+int gcd(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, int smem_optin,
                     int smem_per_sm, Resolved *r) {
   pa_status_t st = check_problem(p);
@@ -132,16 +142,21 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
   r->mma = math == PA_MATH_MMA;
   r->nh_inst = r->mma ? kMaxHeads : simt_heads_instance(r->nh_unit);
   pl.math = math;
-  pl.tile_tokens = tile_tokens(p->head_dim, r->mma);
+  if (o && o->tile_tokens && !tile_supported(p->head_dim, o->tile_tokens))
+    return PA_ERR_UNSUPPORTED;
+  pl.tile_tokens = tile_tokens(p->head_dim, o ? o->tile_tokens : 0);
 
   const int stage_bytes = pl.tile_tokens * p->head_dim * 4;
-  // Two 16 KB stages per warp already keep ~64 KB per SM in flight, which saturates HBM
-  // for this scattered access pattern; deeper rings only add queueing (measured on GB300).
-  int stages = (o && o->stages) ? o->stages : (stage_bytes >= 16384 ? 2 : 4);
-  int per_warp = warp_smem_bytes(p->head_dim, r->mma, r->nh_inst, stages);
-  int warps = (o && o->warps_per_cta) ? o->warps_per_cta
-                                      : std::min(kMaxWarpsPerCta,
-                                                 (smem_optin - kSmemAlign - kStaticSmem) / per_warp);
+  // Measured on GB300: eight warps per SM with 16 KB in flight each (one 16 KB stage, or
+  // two 8 KB ones) saturate HBM for this scattered access pattern; deeper rings only add
+  // queueing.
+  int stages = (o && o->stages) ? o->stages : std::max(1, 16384 / stage_bytes);
+  int per_warp = warp_smem_bytes(p->head_dim, r->mma, r->nh_inst, stages, pl.tile_tokens);
+  // Eight warps per CTA: with all of them on neighbouring K/V heads (group below) their
+  // reads of a row cover up to 8 * head_dim * 2 contiguous bytes.
+  int warps = (o && o->warps_per_cta)
+                  ? o->warps_per_cta
+                  : std::min(kDefaultWarps, (smem_optin - kSmemAlign - kStaticSmem) / per_warp);
   if (warps < 1) return PA_ERR_UNSUPPORTED;
   if (warps * per_warp + kSmemAlign + kStaticSmem > smem_optin) return PA_ERR_UNSUPPORTED;
   const int smem = warps * per_warp + kSmemAlign;
@@ -160,12 +175,17 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
                                                                             : PA_SCHEDULE_BALANCED;
   }
   pl.schedule = sched;
+  // Warps of a CTA are grouped onto neighbouring units (K/V heads) of one sequence and
+  // walk the same tokens, so their K/V reads of a row arrive together and cover
+  // group * head_dim * 2 contiguous bytes.
+  pl.group = gcd(p->kv_heads * r->sub, warps);
   if (sched == PA_SCHEDULE_SINGLE) {
     pl.workers = units;
     pl.combine = PA_COMBINE_FUSED;
     pl.workspace_bytes = 0;
   } else {
     pl.workers = (o && o->workers) ? o->workers : capacity;
+    pl.workers = (pl.workers + pl.group - 1) / pl.group * pl.group;
     pl.combine = o ? o->combine : PA_COMBINE_AUTO;
     if (pl.combine == PA_COMBINE_AUTO) {
       // With more units than workers most units are whole in one worker and the few shared
@@ -304,9 +324,11 @@ void fill_args(KernelArgs *a, const pa_problem_t *p, const Resolved &r, const vo
   a->sub = r.sub;
   a->nh_unit = r.nh_unit;
   a->ups = p->kv_heads * r.sub;
+  a->group = r.plan.group;
+  a->upg = a->ups / a->group;
   a->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a->stages = r.plan.stages;
-  a->warp_smem = warp_smem_bytes(p->head_dim, r.mma, r.nh_inst, r.plan.stages);
+  a->warp_smem = warp_smem_bytes(p->head_dim, r.mma, r.nh_inst, r.plan.stages, r.plan.tile_tokens);
   a->err = device_error_word();
 }
 
@@ -362,7 +384,7 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
   fill_args(&a, p, r, q, bt, ctx, scale, out);
   if (!a.err) return PA_ERR_CUDA;
   a.mode = pl.schedule == PA_SCHEDULE_SINGLE ? MODE_SINGLE : MODE_BALANCED;
-  a.workers = pl.workers;
+  a.workers = pl.workers / pl.group;
   a.fused = pl.combine == PA_COMBINE_FUSED;
   if (a.mode == MODE_BALANCED) {
     const int64_t units = pl.units;
@@ -387,7 +409,7 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
       if (st != PA_OK) return st;
     }
   }
-  if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, pl.ctas, pl.warps_per_cta,
+  if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, r.plan.tile_tokens, pl.ctas, pl.warps_per_cta,
                     static_cast<size_t>(pl.smem_bytes), stream) != cudaSuccess)
     return PA_ERR_CUDA;
   if (a.mode == MODE_BALANCED && !a.fused) {
@@ -498,7 +520,7 @@ pa_status_t pa_split_kv_partial(const pa_problem_t *problem, const void *query,
   a.p_sum = partial_sum;
   a.p_out = partial_out;
   const int ctas = static_cast<int>((workers + r.plan.warps_per_cta - 1) / r.plan.warps_per_cta);
-  if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, ctas, r.plan.warps_per_cta,
+  if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, r.plan.tile_tokens, ctas, r.plan.warps_per_cta,
                     static_cast<size_t>(r.plan.smem_bytes),
                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;

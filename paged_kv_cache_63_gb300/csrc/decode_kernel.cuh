@@ -71,7 +71,7 @@ __device__ __forceinline__ int load_ctx(const KernelArgs &a, int b) {
 // Position of a worker in its token stream.
 struct Cursor {
   int b;         // sequence
-  int us;        // unit within the sequence: kv_head * sub + subgroup
+  int us;        // group unit within the sequence; this warp's unit is us * group + member
   int tok;       // first token of the current tile
   int end;       // exclusive token bound of the current unit segment
   int left;      // tiles still to visit
@@ -82,7 +82,7 @@ struct Cursor {
 __device__ __forceinline__ void next_unit(const KernelArgs &a, Cursor &c, int T) {
   c.ug0 += tiles_of(c.end, T);
   c.tok = 0;
-  if (++c.us == a.ups) {
+  if (++c.us == a.upg) {
     c.us = 0;
     do {
       ++c.b;
@@ -118,19 +118,19 @@ __device__ inline bool balanced_start(const KernelArgs &a, int worker, int T, Cu
     const long long y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  total = __shfl_sync(0xffffffffu, incl, 31) * a.ups;
+  total = __shfl_sync(0xffffffffu, incl, 31) * a.upg;
   nworkers = total < a.workers ? total : a.workers;
   if (worker >= nworkers) return false;
   const long long s = worker_start(worker, total, nworkers);
   const long long e = worker_start(worker + 1, total, nworkers);
   // the lane whose block holds global tile s, then that block walked 32 sequences at a time
-  const int L = __ffs(__ballot_sync(0xffffffffu, incl * a.ups > s)) - 1;
-  long long run = __shfl_sync(0xffffffffu, incl - mine, L) * a.ups;
+  const int L = __ffs(__ballot_sync(0xffffffffu, incl * a.upg > s)) - 1;
+  long long run = __shfl_sync(0xffffffffu, incl - mine, L) * a.upg;
   const int lb0 = min(L * blk, a.batch);
   const int lb1 = min(lb0 + blk, a.batch);
   for (int base = lb0; base < lb1; base += 32) {
     const int b = base + lane;
-    const long long t = b < lb1 ? static_cast<long long>(tiles_of(load_ctx(a, b), T)) * a.ups : 0;
+    const long long t = b < lb1 ? static_cast<long long>(tiles_of(load_ctx(a, b), T)) * a.upg : 0;
     long long in2 = t;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -187,13 +187,13 @@ __device__ __forceinline__ int bt_page(const KernelArgs &a, BtWindow &w, int b, 
 // Issue the TMA loads of the tile at cursor c into a stage (warp-uniform call).
 template <int HD, int T>
 __device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMap *tk,
-                                           const CUtensorMap *tv, const Cursor &c,
+                                           const CUtensorMap *tv, const Cursor &c, int member,
                                            BtWindow &w, uint32_t stage, uint32_t bar,
                                            uint64_t pol) {
   constexpr int kMaxPieces = T / 8;
   const int R = a.ps < T ? a.ps : T;  // rows per piece: a piece never crosses a page
   const int pieces = T / R;
-  const int kv = c.us / a.sub;
+  const int kv = (c.us * a.group + member) / a.sub;
   const int npages = (c.end + a.ps - 1) >> a.ps_shift;
   int row[kMaxPieces];
   uint32_t bytes = 0;
@@ -575,7 +575,7 @@ __device__ __forceinline__ void merge_balanced(const KernelArgs &a, long long un
   if (hl < nh) {
     for (int k = lane & 3; k < n; k += 4) {
       const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-          a.ws_ml + (slot_of(unit, c0 + k) * kMaxHeads + hl) * 2));
+          a.ws_ml + (slot_of(unit, c0 + k, a.group) * kMaxHeads + hl) * 2));
       if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
   }
@@ -600,7 +600,7 @@ __device__ __forceinline__ void merge_balanced(const KernelArgs &a, long long un
     }
 #pragma unroll(HD >= 256 ? 1 : 2)
     for (int k = 0; k < n; ++k) {
-      const long long slot = slot_of(unit, c0 + k);
+      const long long slot = slot_of(unit, c0 + k, a.group);
       const float *ml = a.ws_ml + (slot * kMaxHeads + g0) * 2;
       const float *acc = a.ws_acc + (slot * kMaxHeads + g0) * HD + lane * DPL;
 #pragma unroll
@@ -735,9 +735,9 @@ struct Epilogue<HD, false, NH> {
 // Warm L2 with the query rows of the unit at cursor c (used when the consuming cursor
 // reaches that unit a few tiles later).
 template <int HD>
-__device__ __forceinline__ void prefetch_q(const KernelArgs &a, const Cursor &c) {
+__device__ __forceinline__ void prefetch_q(const KernelArgs &a, const Cursor &c, int member) {
   const int lane = threadIdx.x & 31;
-  const UnitInfo u = unit_info(a, c.b, c.us);
+  const UnitInfo u = unit_info(a, c.b, c.us * a.group + member);
   const int lines = u.nh * HD * 2 / 128;
   if (lane < lines) {
     const uint16_t *p = a.q + (static_cast<long long>(c.b) * a.qh + u.h0) * HD + lane * 64;
@@ -763,7 +763,10 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   __shared__ __align__(8) uint64_t bars[kMaxWarpsPerCta * kMaxStages];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int worker = blockIdx.x * (blockDim.x >> 5) + warp;
+  // warps [group * w, group * (w + 1)) of the grid form worker w; member m serves unit
+  // group_unit * group + m of the worker's group units
+  const int worker = (blockIdx.x * (blockDim.x >> 5) + warp) / a.group;
+  const int member = warp % a.group;
   const int S = a.stages;
   const uint32_t wbase =
       ((smem_addr(dsm) + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1)) +
@@ -779,7 +782,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   // ---- the worker's range
   Cursor c;
   long long total = 0, nworkers = 0;
-  const int units = a.batch * a.ups;
+  const int gunits = a.batch * a.upg;
   if (a.mode == MODE_BALANCED) {
     if (worker >= a.workers) return;
     const bool any = balanced_start(a, worker, T, c, total, nworkers);
@@ -792,7 +795,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
         const int j = __ffs(empty) - 1;
         empty &= empty - 1;
         const int b = static_cast<int>(base + static_cast<long long>(j) * a.workers);
-        for (int us = 0; us < a.ups; ++us) {
+        for (int us = member; us < a.ups; us += a.group) {
           zero_unit<HD>(a, unit_info(a, b, us));
           if (!a.fused && lane == 0) {
             a.ws_info[2 * (b * a.ups + us)] = 0;
@@ -803,23 +806,23 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     }
     if (!any) return;
   } else if (a.mode == MODE_SINGLE) {
-    if (worker >= units) return;
-    c.b = worker / a.ups;
-    c.us = worker % a.ups;
+    if (worker >= gunits) return;
+    c.b = worker / a.upg;
+    c.us = worker % a.upg;
     c.end = load_ctx(a, c.b);
     c.tok = 0;
     c.left = tiles_of(c.end, T);
     c.ug0 = 0;
     if (c.left == 0) {
-      zero_unit<HD>(a, unit_info(a, c.b, c.us));
+      zero_unit<HD>(a, unit_info(a, c.b, c.us * a.group + member));
       return;
     }
   } else {  // MODE_SPLIT
-    if (worker >= units * a.num_splits) return;
+    if (worker >= gunits * a.num_splits) return;
     const int u = worker / a.num_splits;
     const int sp = worker % a.num_splits;
-    c.b = u / a.ups;
-    c.us = u % a.ups;
+    c.b = u / a.upg;
+    c.us = u % a.upg;
     const int ctx = load_ctx(a, c.b);
     const int pages = (ctx + a.ps - 1) >> a.ps_shift;
     const int pps = (pages + a.num_splits - 1) / a.num_splits;
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     c.left = c.end > c.tok ? tiles_of(c.end - c.tok, T) : 0;
     c.ug0 = 0;
     if (c.left == 0) {
-      const UnitInfo ui = unit_info(a, c.b, c.us);
+      const UnitInfo ui = unit_info(a, c.b, c.us * a.group + member);
       const long long row = (static_cast<long long>(c.b) * a.num_splits + sp) * a.qh + ui.h0;
       for (int h = 0; h < ui.nh; ++h) {
         if (lane == 0) {
@@ -861,7 +864,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   win.cur = win.nxt = -1;
   int issued = 0, consumed = 0;
   for (; issued < S - 1 && ic.left > 0; ++issued) {
-    issue_tile<HD, T>(a, &tk, &tv, ic, win, wbase + issued * G::kStageBytes, bar0 + 8 * issued, pol);
+    issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + issued * G::kStageBytes, bar0 + 8 * issued, pol);
     advance(a, ic, T);
   }
 
@@ -900,7 +903,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
       Ep::final_out(a, st, cur);
       return;
     }
-    const long long slot = slot_of(unit, worker);
+    const long long slot = slot_of(unit, worker, a.group);
     Ep::partial_out(st, cur, a.ws_ml + slot * kMaxHeads * 2, a.ws_ml + slot * kMaxHeads * 2 + 1,
                     a.ws_acc + slot * kMaxHeads * HD, 2, HD);
     if (!a.fused) return;
@@ -918,9 +921,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
 
   // ---- main loop: refill the slot freed last iteration, wait for the next tile, compute
   while (c.left > 0) {
-    if (c.b != cur.b || c.us != cur.us) {
+    if (c.b != cur.b || c.us * a.group + member != cur.us) {
       if (cur.b >= 0) finish_unit();
-      cur = unit_info(a, c.b, c.us);
+      cur = unit_info(a, c.b, c.us * a.group + member);
       cur_ug0 = c.ug0;
       cur_end = c.end;
       if constexpr (MMA)
@@ -930,11 +933,11 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     }
     if (ic.left > 0) {
       const int s = issued % S;
-      issue_tile<HD, T>(a, &tk, &tv, ic, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol);
+      issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol);
       ++issued;
       const int ib = ic.b, ius = ic.us;
       advance(a, ic, T);
-      if (ic.left > 0 && (ic.b != ib || ic.us != ius)) prefetch_q<HD>(a, ic);
+      if (ic.left > 0 && (ic.b != ib || ic.us != ius)) prefetch_q<HD>(a, ic, member);
     }
     const int s = consumed % S;
     if (!mbar_wait(bar0 + 8 * s, static_cast<uint32_t>((consumed / S) & 1), a.err)) {
@@ -986,7 +989,7 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant
   float mx = -INFINITY;
   for (int k = tid; k < n; k += 256) {
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-        a.ws_ml + (slot_of(unit, c0 + k) * kMaxHeads + h) * 2));
+        a.ws_ml + (slot_of(unit, c0 + k, a.group) * kMaxHeads + h) * 2));
     if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
   }
 #pragma unroll
@@ -1002,7 +1005,7 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant
   float L = 0.f;
 #pragma unroll 2
   for (int k = warp; k < n; k += 8) {
-    const long long slot = slot_of(unit, c0 + k);
+    const long long slot = slot_of(unit, c0 + k, a.group);
     const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
     const float w = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
     L += w * ml.y;

@@ -6,15 +6,12 @@
 
 namespace pa {
 
-template <int HD>
-constexpr int kTileTokens = HD >= 256 ? 16 : 32;
-
 constexpr int kMaxDevices = 64;
 
-template <int HD, bool MMA, int NH>
+template <int HD, int T, bool MMA, int NH>
 cudaError_t launch_variant(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                            int ctas, int warps, size_t smem, cudaStream_t stream) {
-  auto kern = decode_kernel<HD, kTileTokens<HD>, MMA, NH>;
+  auto kern = decode_kernel<HD, T, MMA, NH>;
   // the opt-in shared-memory size is a per-device function attribute; remember the
   // largest value set on each device
   static int smem_set[kMaxDevices] = {0};
@@ -31,19 +28,35 @@ cudaError_t launch_variant(const KernelArgs &a, const CUtensorMap *tk, const CUt
   return cudaGetLastError();
 }
 
-template <int HD>
-cudaError_t launch_decode_hd(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+template <int HD, int T>
+cudaError_t launch_decode_ht(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                              int mma, int nh_inst, int ctas, int warps, size_t smem,
                              cudaStream_t stream) {
-  if (mma) return launch_variant<HD, true, kMaxHeads>(a, tk, tv, ctas, warps, smem, stream);
+  if (mma) return launch_variant<HD, T, true, kMaxHeads>(a, tk, tv, ctas, warps, smem, stream);
   switch (nh_inst) {
-    case 1: return launch_variant<HD, false, 1>(a, tk, tv, ctas, warps, smem, stream);
-    case 2: return launch_variant<HD, false, 2>(a, tk, tv, ctas, warps, smem, stream);
-    case 4: return launch_variant<HD, false, 4>(a, tk, tv, ctas, warps, smem, stream);
-    case 6: return launch_variant<HD, false, 6>(a, tk, tv, ctas, warps, smem, stream);
-    case 8: return launch_variant<HD, false, 8>(a, tk, tv, ctas, warps, smem, stream);
+    case 1: return launch_variant<HD, T, false, 1>(a, tk, tv, ctas, warps, smem, stream);
+    case 2: return launch_variant<HD, T, false, 2>(a, tk, tv, ctas, warps, smem, stream);
+    case 4: return launch_variant<HD, T, false, 4>(a, tk, tv, ctas, warps, smem, stream);
+    case 6: return launch_variant<HD, T, false, 6>(a, tk, tv, ctas, warps, smem, stream);
+    case 8: return launch_variant<HD, T, false, 8>(a, tk, tv, ctas, warps, smem, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Tile sizes instantiated per head_dim: 32 tokens for 64, 16 or 32 for 128, 16 for 256.
+template <int HD>
+cudaError_t launch_decode_hd(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
+                             int mma, int nh_inst, int tile, int ctas, int warps, size_t smem,
+                             cudaStream_t stream) {
+  if constexpr (HD == 64) {
+    if (tile == 32) return launch_decode_ht<HD, 32>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);
+  } else if constexpr (HD == 128) {
+    if (tile == 16) return launch_decode_ht<HD, 16>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);
+    if (tile == 32) return launch_decode_ht<HD, 32>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);
+  } else {
+    if (tile == 16) return launch_decode_ht<HD, 16>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int HD>
@@ -77,9 +90,9 @@ cudaError_t launch_combine_split_hd(const KernelArgs &a, cudaStream_t stream) {
 #define PA_INSTANTIATE_HD(HD)                                                                \
   namespace pa {                                                                             \
   cudaError_t launch_decode_hd##HD(const KernelArgs &a, const CUtensorMap *tk,               \
-                                   const CUtensorMap *tv, int mma, int nh_inst, int ctas,    \
-                                   int warps, size_t smem, cudaStream_t stream) {            \
-    return launch_decode_hd<HD>(a, tk, tv, mma, nh_inst, ctas, warps, smem, stream);         \
+                                   const CUtensorMap *tv, int mma, int nh_inst, int tile,    \
+                                   int ctas, int warps, size_t smem, cudaStream_t stream) {  \
+    return launch_decode_hd<HD>(a, tk, tv, mma, nh_inst, tile, ctas, warps, smem, stream);   \
   }                                                                                          \
   cudaError_t launch_combine_balanced_hd##HD(const KernelArgs &a, int units, int heads,      \
                                              cudaStream_t stream) {                          \

@@ -46,10 +46,13 @@ struct KernelArgs {
   int sub;      // units per K/V head
   int nh_unit;  // heads per unit (ceil(g / sub))
   int ups;      // units per sequence = kvh * sub
+  int group;    // warps per worker; warp `member` of a worker serves unit group_unit * group +
+                // member, so the warps of a worker read neighbouring K/V heads together
+  int upg;      // group units per sequence = ups / group
   float scale_log2;  // scale * log2(e)
   int mode;
   int num_splits;  // MODE_SPLIT
-  int workers;     // MODE_BALANCED: number of workers
+  int workers;     // MODE_BALANCED: number of workers (groups of `group` warps)
   int fused;       // MODE_BALANCED: last worker merges
   int stages;
   int warp_smem;   // bytes of dynamic shared memory per warp (multiple of kSmemAlign)
@@ -73,22 +76,28 @@ PA_HD int64_t worker_of(int64_t x, int64_t total, int64_t workers) {
   return ((x + 1) * workers - 1) / total;
 }
 
-// Partial-state slot of (unit u, worker c): along the monotone path of (unit, worker)
-// pairs in tile order each step raises u or c, so u + c is unique; slots < units + workers.
-PA_HD int64_t slot_of(int64_t unit, int64_t worker) { return unit + worker; }
+// Partial-state slot of (unit u, worker c) when workers are groups of `group` warps that
+// serve `group` consecutive units of a sequence (unit u = group_unit * group + member).
+// Along the monotone path of (group_unit, worker) pairs in tile order each step raises one
+// of them, so group_unit + c is unique per member and (group_unit + c) * group + member
+// = u + c * group is unique; slots < units + workers * group.
+PA_HD int64_t slot_of(int64_t unit, int64_t worker, int64_t group) { return unit + worker * group; }
 
 // ---- launchers (defined in the .cu files) --------------------------------------------
 
-int tile_tokens(int head_dim, int mma);
-// Dynamic shared memory one worker warp needs (multiple of kSmemAlign).
-int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages);
+// Tokens per K/V tile for head_dim: `requested` when that size is instantiated, else the
+// default (32, or 16 for head_dim 256).
+int tile_tokens(int head_dim, int requested);
+bool tile_supported(int head_dim, int tile);
+// Dynamic shared memory one warp needs (multiple of kSmemAlign).
+int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages, int tile);
 // SIMT kernels are instantiated for these head counts per unit; returns the smallest
 // instantiation >= nh.
 int simt_heads_instance(int nh);
 
 cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
-                          int mma, int nh_inst, int ctas, int warps_per_cta, size_t smem,
-                          cudaStream_t stream);
+                          int mma, int nh_inst, int tile, int ctas, int warps_per_cta,
+                          size_t smem, cudaStream_t stream);
 cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads,
                                     cudaStream_t stream);
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);

@@ -6,11 +6,11 @@
 namespace pa {
 
 cudaError_t launch_decode_hd64(const KernelArgs &, const CUtensorMap *, const CUtensorMap *, int,
-                               int, int, int, size_t, cudaStream_t);
+                               int, int, int, int, size_t, cudaStream_t);
 cudaError_t launch_decode_hd128(const KernelArgs &, const CUtensorMap *, const CUtensorMap *, int,
-                                int, int, int, size_t, cudaStream_t);
+                                int, int, int, int, size_t, cudaStream_t);
 cudaError_t launch_decode_hd256(const KernelArgs &, const CUtensorMap *, const CUtensorMap *, int,
-                                int, int, int, size_t, cudaStream_t);
+                                int, int, int, int, size_t, cudaStream_t);
 cudaError_t launch_combine_balanced_hd64(const KernelArgs &, int, int, cudaStream_t);
 cudaError_t launch_combine_balanced_hd128(const KernelArgs &, int, int, cudaStream_t);
 cudaError_t launch_combine_balanced_hd256(const KernelArgs &, int, int, cudaStream_t);
@@ -21,7 +21,14 @@ cudaError_t launch_combine_split_hd256(const KernelArgs &, cudaStream_t);
 // One word per device: PA_DEVERR_* bits raised by the kernels.
 __device__ unsigned g_device_error = 0;
 
-int tile_tokens(int head_dim, int /*mma*/) { return head_dim >= 256 ? 16 : 32; }
+int tile_tokens(int head_dim, int requested) {
+  if (head_dim == 128 && (requested == 16 || requested == 32)) return requested;
+  return head_dim >= 256 ? 16 : 32;
+}
+
+bool tile_supported(int head_dim, int tile) {
+  return tile == tile_tokens(head_dim, tile);
+}
 
 int simt_heads_instance(int nh) {
   if (nh <= 1) return 1;
@@ -31,8 +38,7 @@ int simt_heads_instance(int nh) {
   return 8;
 }
 
-int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages) {
-  const int t = tile_tokens(head_dim, mma);
+int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages, int t) {
   long long bytes = static_cast<long long>(stages) * t * head_dim * 4;
   if (!mma) {
     const int nhp = (nh_inst + 3) & ~3;
@@ -43,12 +49,15 @@ int warp_smem_bytes(int head_dim, int mma, int nh_inst, int stages) {
 }
 
 cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
-                          int mma, int nh_inst, int ctas, int warps_per_cta, size_t smem,
-                          cudaStream_t stream) {
+                          int mma, int nh_inst, int tile, int ctas, int warps_per_cta,
+                          size_t smem, cudaStream_t stream) {
   switch (a.hd) {
-    case 64: return launch_decode_hd64(a, tk, tv, mma, nh_inst, ctas, warps_per_cta, smem, stream);
-    case 128: return launch_decode_hd128(a, tk, tv, mma, nh_inst, ctas, warps_per_cta, smem, stream);
-    case 256: return launch_decode_hd256(a, tk, tv, mma, nh_inst, ctas, warps_per_cta, smem, stream);
+    case 64:
+      return launch_decode_hd64(a, tk, tv, mma, nh_inst, tile, ctas, warps_per_cta, smem, stream);
+    case 128:
+      return launch_decode_hd128(a, tk, tv, mma, nh_inst, tile, ctas, warps_per_cta, smem, stream);
+    case 256:
+      return launch_decode_hd256(a, tk, tv, mma, nh_inst, tile, ctas, warps_per_cta, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -51,7 +51,7 @@ class pa_options_t(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int32), ("math", ctypes.c_int32),
                 ("combine", ctypes.c_int32), ("workers", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("tile_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class pa_plan_t(ctypes.Structure):
@@ -60,6 +60,7 @@ class pa_plan_t(ctypes.Structure):
                 ("warps_per_cta", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
                 ("units", ctypes.c_int32), ("heads_per_unit", ctypes.c_int32),
+                ("group", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
 
@@ -117,12 +118,13 @@ def problem_of(w) -> pa_problem_t:
 
 
 def options(schedule="auto", math="auto", combine="auto", workers=0, stages=0,
-            warps_per_cta=0) -> pa_options_t:
+            warps_per_cta=0, tile_tokens=0) -> pa_options_t:
     o = pa_options_t()
     o.schedule = SCHEDULE[schedule] if isinstance(schedule, str) else int(schedule)
     o.math = MATH[math] if isinstance(math, str) else int(math)
     o.combine = COMBINE[combine] if isinstance(combine, str) else int(combine)
     o.workers, o.stages, o.warps_per_cta = int(workers), int(stages), int(warps_per_cta)
+    o.tile_tokens = int(tile_tokens)
     return o
 
 

@@ -102,7 +102,8 @@ def test_plan_heuristic():
     assert pl["schedule"] == 1 and pl["workspace_bytes"] == 0 and pl["workers"] == 4096 * 8
     # forced options are honoured
     pl = lib.pa_plan(P(), lib.options(schedule="balanced", workers=7, combine="kernel"))
-    assert (pl["schedule"], pl["workers"], pl["combine"]) == (2, 7, 2)
+    assert (pl["schedule"], pl["combine"]) == (2, 2)
+    assert pl["workers"] % pl["group"] == 0 and 7 <= pl["workers"] < 7 + pl["group"]
     # many workers per unit: the separate combine kernel; few: the fused merge
     pl = lib.pa_plan(P(batch=4, query_heads=24, kv_heads=4, head_dim=256, page_size=64,
                        max_pages_per_sequence=1563, num_physical_pages=6252))
@@ -155,14 +156,16 @@ using namespace pa;
 int main() {
   srand(7);
   for (int trial = 0; trial < 400; ++trial) {
-    int batch = 1 + rand() % 40, ups = 1 + rand() % 9, T = (rand() % 2) ? 16 : 32;
+    // G warps per worker serve G consecutive units; units = group units * G
+    int batch = 1 + rand() % 40, G = 1 << (rand() % 3), upg = 1 + rand() % 5, T = (rand() % 2) ? 16 : 32;
+    int ups = upg * G;
     int workers = 1 + rand() % 700;
     std::vector<int> ctx(batch);
     for (auto &c : ctx) c = (rand() % 4 == 0) ? 0 : 1 + rand() % 3000;
     long long total = 0;
-    std::vector<long long> u0, u1;
+    std::vector<long long> u0, u1;  // tile range of each group unit
     for (int b = 0; b < batch; ++b)
-      for (int u = 0; u < ups; ++u) {
+      for (int u = 0; u < upg; ++u) {
         u0.push_back(total);
         total += tiles_of(ctx[b], T);
         u1.push_back(total);
@@ -183,16 +186,19 @@ int main() {
       if (worker_of(x, total, workers) != owner[x]) { printf("worker_of wrong\n"); return 1; }
     }
     std::set<long long> slots;
-    for (size_t u = 0; u < u0.size(); ++u) {
-      if (u0[u] == u1[u]) continue;
-      long long c0 = worker_of(u0[u], total, workers), c1 = worker_of(u1[u] - 1, total, workers);
+    const long long units = (long long)u0.size() * G;
+    for (size_t gu = 0; gu < u0.size(); ++gu) {
+      if (u0[gu] == u1[gu]) continue;
+      long long c0 = worker_of(u0[gu], total, workers), c1 = worker_of(u1[gu] - 1, total, workers);
       for (long long c = c0; c <= c1; ++c) {
-        // every worker from the first to the last holds tiles of this unit
-        if (worker_start(c, total, workers) >= u1[u] || worker_start(c + 1, total, workers) <= u0[u]) {
+        // every worker from the first to the last holds tiles of this group unit
+        if (worker_start(c, total, workers) >= u1[gu] || worker_start(c + 1, total, workers) <= u0[gu]) {
           printf("gap in contributors\n"); return 1; }
-        long long s = slot_of((long long)u, c);
-        if (!slots.insert(s).second || s >= (long long)u0.size() + workers) {
-          printf("slot clash\n"); return 1; }
+        for (int m = 0; m < G; ++m) {
+          long long s = slot_of((long long)gu * G + m, c, G);
+          if (!slots.insert(s).second || s >= units + (long long)workers * G) {
+            printf("slot clash\n"); return 1; }
+        }
       }
     }
   }

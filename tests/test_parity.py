@@ -116,3 +116,17 @@ def test_full_size_sampled(name):
         for h in range(w.query_heads):
             v = w.value_cache[page, 0, h // g].astype(np.float32)
             assert np.array_equal(got[b * w.query_heads + h], v)
+
+
+HD128 = ["mid_small", "mha_small", "ragged_small", "g12", "ps256"]
+
+
+@pytest.mark.parametrize("opt", ["mma-single", "mma-balanced", "simt-balanced-kernel"])
+@pytest.mark.parametrize("name", HD128)
+def test_tile16_parity(name, opt):
+    """head_dim 128 with 16-token tiles (the other instantiated tile size)."""
+    w, ref = case(name)
+    got = run(w, opts=lib.options(tile_tokens=16, **OPTS[opt]))
+    assert_close(got, ref, f"{name}/{opt}/t16")
+    assert lib.status_of(lib.pa_plan, lib.problem_of(make_workload("long_gqa6")),
+                         lib.options(tile_tokens=32)) == 2

@@ -136,28 +136,25 @@ def test_side_stream():
 
 def test_workspace_follows_shape_changes():
     """One workspace (library-owned, and one caller buffer) across problems whose unit
-    counts grow and shrink: merge counters must start at zero every time."""
+    counts grow and shrink, with the caller buffer's calls alternating between the fused
+    merge and the combine kernel: merge counters must start at zero every time."""
     import oracle
 
     t = torch()
-    # long_gqa6 has few units and takes the separate combine kernel, whose partial states
-    # land where a later fused call keeps its counters
-    seq = [make_workload("gqa4_mid", batch=3), make_workload("ragged", batch=20),
-           make_workload("long_gqa6", context_lengths=[3000, 500]),
-           make_workload("gqa4_mid", batch=5), make_workload("ragged", batch=30),
-           make_workload("tiny"), make_workload("long_gqa6", context_lengths=[900]),
-           make_workload("ragged", batch=30)]
+    seq = [make_workload("ragged", batch=100), make_workload("gqa4_mid", batch=3),
+           make_workload("ragged", batch=120), make_workload("long_gqa6", context_lengths=[3000, 500]),
+           make_workload("ragged", batch=90), make_workload("tiny"),
+           make_workload("long_gqa6", context_lengths=[900]), make_workload("ragged", batch=130)]
     refs = [oracle.decode(w) for w in seq]
-    for w, ref in zip(seq, refs):  # library-owned workspace (pa_decode)
+    for w, ref in zip(seq, refs):  # library-owned workspace (pa_decode), the plan's merge
         assert_close(run(w), ref, f"pa_decode {w.name} b={w.batch}")
-    opts = lib.options(schedule="balanced")
-    assert {lib.pa_plan(lib.problem_of(w), opts)["combine"] for w in seq} == {1, 2}
-    n = max(lib.pa_workspace_size(lib.problem_of(w), opts) for w in seq)
+    combos = [lib.options(schedule="balanced", combine=c) for c in ("fused", "kernel")]
+    n = max(lib.pa_workspace_size(lib.problem_of(w), o) for w in seq for o in combos)
     ws = t.empty(n, dtype=t.uint8, device="cuda")
     lib.pa_workspace_init(ws, n)
-    for w, ref in zip(seq, refs):
+    for i, (w, ref) in enumerate(zip(seq, refs)):
         d = to_device(w)
         lib.pa_decode_ex(lib.problem_of(w), d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale,
-                         d["out"], opts, ws, n)
+                         d["out"], combos[i % 2], ws, n)
         t.cuda.synchronize()
         assert_close(d["out"].cpu().numpy(), ref, f"pa_decode_ex {w.name} b={w.batch}")
