@@ -111,8 +111,14 @@ typedef struct pa_options_t {
   int32_t stages;      /* K/V pipeline depth per worker; 0 = default */
   int32_t warps_per_cta; /* 0 = default */
   int32_t tile_tokens; /* tokens per K/V tile: 0 = default; 16 or 32 for head_dim 128 */
-  int32_t reserved[1]; /* must be 0 */
+  int32_t test_flags;  /* 0, or PA_TEST_EXPIRE_WAITS (tests of failure detection only) */
 } pa_options_t;
+
+/* Test hook for the failure path: every warp's first K/V tile waits for 16 bytes that never
+ * arrive, so its bounded wait runs out (after about a second), the call raises
+ * PA_DEVERR_TIMEOUT and its outputs are invalid; the device stays usable. A workspace used by
+ * such a call must be re-initialised with pa_workspace_init. */
+#define PA_TEST_EXPIRE_WAITS 1
 
 /* What pa_decode / pa_decode_ex will launch for a problem (filled by pa_plan). */
 typedef struct pa_plan_t {

@@ -57,7 +57,8 @@ pa_status_t check_options(const pa_options_t *o) {
   if (o->math < PA_MATH_AUTO || o->math > PA_MATH_MMA) return PA_ERR_INVALID_ARG;
   if (o->combine < PA_COMBINE_AUTO || o->combine > PA_COMBINE_KERNEL) return PA_ERR_INVALID_ARG;
   if (o->workers < 0 || o->stages < 0 || o->stages > kMaxStages || o->warps_per_cta < 0 ||
-      o->warps_per_cta > kMaxWarpsPerCta || o->tile_tokens < 0 || o->reserved[0])
+      o->warps_per_cta > kMaxWarpsPerCta || o->tile_tokens < 0 ||
+      (o->test_flags & ~PA_TEST_EXPIRE_WAITS))
     return PA_ERR_INVALID_ARG;
   return PA_OK;
 }
@@ -385,6 +386,7 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
   if (!a.err) return PA_ERR_CUDA;
   a.mode = pl.schedule == PA_SCHEDULE_SINGLE ? MODE_SINGLE : MODE_BALANCED;
   a.workers = pl.workers / pl.group;
+  if (o && (o->test_flags & PA_TEST_EXPIRE_WAITS)) a.tx_extra = 16;
   a.fused = pl.combine == PA_COMBINE_FUSED;
   if (a.mode == MODE_BALANCED) {
     const int64_t units = pl.units;

@@ -189,7 +189,7 @@ template <int HD, int T>
 __device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMap *tk,
                                            const CUtensorMap *tv, const Cursor &c, int member,
                                            BtWindow &w, uint32_t stage, uint32_t bar,
-                                           uint64_t pol) {
+                                           uint64_t pol, uint32_t extra_tx) {
   constexpr int kMaxPieces = T / 8;
   const int R = a.ps < T ? a.ps : T;  // rows per piece: a piece never crosses a page
   const int pieces = T / R;
@@ -212,7 +212,7 @@ __device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMa
     }
   }
   if ((threadIdx.x & 31) == 0) {
-    mbar_arrive_expect_tx(bar, bytes);
+    mbar_arrive_expect_tx(bar, bytes + extra_tx);
 #pragma unroll
     for (int p = 0; p < kMaxPieces; ++p) {
       if (row[p] < 0) continue;
@@ -864,7 +864,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   win.cur = win.nxt = -1;
   int issued = 0, consumed = 0;
   for (; issued < S - 1 && ic.left > 0; ++issued) {
-    issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + issued * G::kStageBytes, bar0 + 8 * issued, pol);
+    issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + issued * G::kStageBytes, bar0 + 8 * issued, pol,
+                      issued == 0 ? a.tx_extra : 0u);
     advance(a, ic, T);
   }
 
@@ -933,7 +934,8 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     }
     if (ic.left > 0) {
       const int s = issued % S;
-      issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol);
+      issue_tile<HD, T>(a, &tk, &tv, ic, member, win, wbase + s * G::kStageBytes, bar0 + 8 * s, pol,
+                        issued == 0 ? a.tx_extra : 0u);
       ++issued;
       const int ib = ic.b, ius = ic.us;
       advance(a, ic, T);
@@ -977,7 +979,8 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant
   const int h = blockIdx.y;
   const int c0 = a.ws_info[2 * unit];
   const int n = a.ws_info[2 * unit + 1];
-  if (n <= 1) return;
+  // entries left by a call that did not finish are skipped, never followed out of range
+  if (n <= 1 || c0 < 0 || n > a.workers || c0 > a.workers - n) return;
   const UnitInfo u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
   if (h >= u.nh) return;
   __shared__ float s_max[8];

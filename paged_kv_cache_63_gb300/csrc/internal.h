@@ -56,6 +56,8 @@ struct KernelArgs {
   int fused;       // MODE_BALANCED: last worker merges
   int stages;
   int warp_smem;   // bytes of dynamic shared memory per warp (multiple of kSmemAlign)
+  unsigned tx_extra;  // bytes the first tile of each warp waits for beyond what it loads
+                      // (nonzero only under PA_TEST_EXPIRE_WAITS)
 };
 
 // ---- schedule arithmetic shared by the kernels and the host-side checks -------------

@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 PA_DEVERR_PAGE_ID = 1
 PA_DEVERR_CONTEXT = 2
 PA_DEVERR_TIMEOUT = 4
+PA_TEST_EXPIRE_WAITS = 1
 SCHEDULE = {"auto": 0, "single": 1, "balanced": 2}
 MATH = {"auto": 0, "simt": 1, "mma": 2}
 COMBINE = {"auto": 0, "fused": 1, "kernel": 2}
@@ -51,7 +52,7 @@ class pa_options_t(ctypes.Structure):
     _fields_ = [("schedule", ctypes.c_int32), ("math", ctypes.c_int32),
                 ("combine", ctypes.c_int32), ("workers", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("warps_per_cta", ctypes.c_int32),
-                ("tile_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("tile_tokens", ctypes.c_int32), ("test_flags", ctypes.c_int32)]
 
 
 class pa_plan_t(ctypes.Structure):
@@ -118,13 +119,14 @@ def problem_of(w) -> pa_problem_t:
 
 
 def options(schedule="auto", math="auto", combine="auto", workers=0, stages=0,
-            warps_per_cta=0, tile_tokens=0) -> pa_options_t:
+            warps_per_cta=0, tile_tokens=0, test_flags=0) -> pa_options_t:
     o = pa_options_t()
     o.schedule = SCHEDULE[schedule] if isinstance(schedule, str) else int(schedule)
     o.math = MATH[math] if isinstance(math, str) else int(math)
     o.combine = COMBINE[combine] if isinstance(combine, str) else int(combine)
     o.workers, o.stages, o.warps_per_cta = int(workers), int(stages), int(warps_per_cta)
     o.tile_tokens = int(tile_tokens)
+    o.test_flags = int(test_flags)
     return o
 
 

@@ -67,9 +67,8 @@ def test_plan_rejects_bad_problems(kw, status):
 def test_plan_rejects_bad_options():
     assert lib.status_of(lib.pa_plan, P(), lib.options(schedule=7)) == 1
     assert lib.status_of(lib.pa_plan, P(), lib.options(stages=99)) == 1
-    o = lib.options()
-    o.reserved[0] = 1
-    assert lib.status_of(lib.pa_plan, P(), o) == 1
+    assert lib.status_of(lib.pa_plan, P(), lib.options(test_flags=2)) == 1
+    assert lib.status_of(lib.pa_plan, P(), lib.options(tile_tokens=-1)) == 1
     assert lib.status_of(lib.pa_plan, P(), None, 0) == 1
 
 

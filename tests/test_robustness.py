@@ -158,3 +158,30 @@ def test_workspace_follows_shape_changes():
                          d["out"], combos[i % 2], ws, n)
         t.cuda.synchronize()
         assert_close(d["out"].cpu().numpy(), ref, f"pa_decode_ex {w.name} b={w.batch}")
+
+
+def test_expired_wait_is_reported_and_device_stays_usable():
+    """Failure detection without a fault: under PA_TEST_EXPIRE_WAITS each warp's first tile
+    waits for bytes that never come; the bounded wait gives up (about a second), the call
+    raises PA_DEVERR_TIMEOUT, and the next call on the same device is correct."""
+    import oracle
+
+    t = torch()
+    w = make_workload("gqa4_mid", batch=4)
+    d = to_device(w)
+    prob = lib.problem_of(w)
+    bad = lib.options(test_flags=lib.PA_TEST_EXPIRE_WAITS)
+    n = lib.pa_workspace_size(prob, bad)
+    ws = t.empty(max(n, 256), dtype=t.uint8, device="cuda")
+    lib.pa_workspace_init(ws, n)
+    lib.pa_decode_ex(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"], bad,
+                     ws, n)
+    t.cuda.synchronize()
+    assert lib.pa_get_device_error() & lib.PA_DEVERR_TIMEOUT
+    assert lib.pa_get_device_error() == 0  # reading clears it
+    lib.pa_workspace_init(ws, n)
+    lib.pa_decode_ex(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"],
+                     lib.options(), ws, n)
+    t.cuda.synchronize()
+    assert lib.pa_get_device_error() == 0
+    assert_close(d["out"].cpu().numpy(), oracle.decode(w), "after an expired wait")
