@@ -15,6 +15,8 @@
  * Data types and layouts (all row-major, C order):
  *   query          fp16  [batch][query_heads][head_dim]
  *   key_cache      fp16  [num_physical_pages][page_size][kv_heads][head_dim]
+ *                        ([num_physical_pages][kv_heads][page_size][head_dim] with
+ *                        cache_layout = PA_LAYOUT_HEAD_MAJOR)
  *   value_cache    fp16  same layout as key_cache
  *   block_tables   int32 [batch][max_pages_per_sequence]; only the first
  *                        ceil(context_lengths[b] / page_size) entries of row b are read
@@ -56,7 +58,17 @@ typedef struct pa_problem_t {
   int32_t max_pages_per_sequence; /* columns of block_tables, >= 1 */
   int32_t num_physical_pages;     /* pages in each cache, >= 1;
                                      num_physical_pages * page_size < 2^31 */
+  int32_t cache_layout;           /* pa_cache_layout_t; 0 (the pages' layout) by default */
 } pa_problem_t;
+
+/* Layout of key_cache and value_cache. TOKEN_MAJOR is the layout of "[TIL] Optimizing paged
+ * attention", section "Data Layout"; HEAD_MAJOR is the alternative that section "V2
+ * (Vectorization)" proposes comparing, in which one K/V head's rows of a page are contiguous
+ * (num_physical_pages * kv_heads < 2^31). */
+typedef enum pa_cache_layout_t {
+  PA_LAYOUT_TOKEN_MAJOR = 0, /* [num_physical_pages][page_size][kv_heads][head_dim] */
+  PA_LAYOUT_HEAD_MAJOR = 1   /* [num_physical_pages][kv_heads][page_size][head_dim] */
+} pa_cache_layout_t;
 
 typedef enum pa_status_t {
   PA_OK = 0,

@@ -54,10 +54,10 @@ def _bind(path: str):
     lib.oracle_half_to_double.restype = ctypes.c_double
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_decode.restype = i32
-    lib.oracle_decode.argtypes = [i32] * 7 + [p] * 5 + [ctypes.c_double, p, ctypes.c_int64, p,
+    lib.oracle_decode.argtypes = [i32] * 8 + [p] * 5 + [ctypes.c_double, p, ctypes.c_int64, p,
                                                       i32]
     lib.oracle_partial.restype = i32
-    lib.oracle_partial.argtypes = [i32] * 7 + [p] * 5 + [ctypes.c_double, ctypes.c_int64, i32,
+    lib.oracle_partial.argtypes = [i32] * 8 + [p] * 5 + [ctypes.c_double, ctypes.c_int64, i32,
                                                        i32, p, p, p]
     lib.oracle_combine.restype = None
     lib.oracle_combine.argtypes = [i32, i32, p, p, p, p]
@@ -85,7 +85,8 @@ def _inputs(w):
     bt = np.ascontiguousarray(w.block_tables, dtype=np.int32)
     ctx = np.ascontiguousarray(w.context_lengths, dtype=np.int32)
     dims = [int(w.batch), int(w.query_heads), int(w.kv_heads), int(w.head_dim),
-            int(w.page_size), int(w.max_pages_per_sequence), int(w.num_physical_pages)]
+            int(w.page_size), int(w.max_pages_per_sequence), int(w.num_physical_pages),
+            int(getattr(w, "cache_layout", 0))]
     return dims, q, k, v, bt, ctx
 
 

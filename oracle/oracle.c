@@ -16,6 +16,10 @@
  * and their sum), in fp64, from fp16 inputs widened exactly; the kernels' online
  * recurrence and split/merge give the same value in exact arithmetic.
  *
+ * Two cache layouts: 0 = [page][slot][kv_head][head_dim] as section "Data Layout" gives it;
+ * 1 = [page][kv_head][slot][head_dim], the alternative layout the pages suggest comparing
+ * (section "V2 (Vectorization)"), where one head's rows of a page are contiguous.
+ *
  * Readings where the pages are silent:
  *   - a context length of 0 yields an all-zero output row (empty sum);
  *   - indices are checked: a context longer than max_pages_per_sequence*page_size,
@@ -48,11 +52,12 @@ double oracle_half_to_double(uint16_t h) {
 }
 
 typedef struct {
-  int batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages;
+  int batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages, layout;
 } dims_t;
 
 /* Element offset of (physical page, slot, kv head, 0) in the cache. */
 static int64_t cache_row(const dims_t *p, int64_t page, int slot, int kv) {
+  if (p->layout == 1) return ((page * p->kv_heads + kv) * (int64_t)p->page_size + slot) * p->head_dim;
   return ((page * p->page_size + slot) * (int64_t)p->kv_heads + kv) * p->head_dim;
 }
 
@@ -82,6 +87,7 @@ static int check_dims(const dims_t *p) {
       p->page_size <= 0 || p->max_pages <= 0 || p->num_pages <= 0)
     return 1;
   if (p->query_heads % p->kv_heads) return 1;
+  if (p->layout != 0 && p->layout != 1) return 1;
   return 0;
 }
 
@@ -127,11 +133,11 @@ static int decode_row(const dims_t *p, const uint16_t *q, const uint16_t *key,
  * listed rows r = b * query_heads + h (out is [n_rows][head_dim]). n_threads <= 0 uses
  * the OpenMP default. Returns 0, or the first nonzero row code. */
 int oracle_decode(int batch, int query_heads, int kv_heads, int head_dim, int page_size,
-                  int max_pages, int num_pages, const uint16_t *query,
+                  int max_pages, int num_pages, int layout, const uint16_t *query,
                   const uint16_t *key_cache, const uint16_t *value_cache,
                   const int32_t *block_tables, const int32_t *context_lengths, double scale,
                   const int64_t *rows, int64_t n_rows, double *out, int n_threads) {
-  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages};
+  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages, layout};
   if (check_dims(&p)) return 1;
   int64_t total = rows ? n_rows : (int64_t)batch * query_heads;
   int status = 0;
@@ -161,12 +167,12 @@ int oracle_decode(int batch, int query_heads, int kv_heads, int head_dim, int pa
  * m = -inf, l = 0, acc = 0.  This is the per-split state of the context-split scheme in
  * "[TIL] Optimizing paged attention", section "V4 (Context-axis parallelism)". */
 int oracle_partial(int batch, int query_heads, int kv_heads, int head_dim, int page_size,
-                   int max_pages, int num_pages, const uint16_t *query,
+                   int max_pages, int num_pages, int layout, const uint16_t *query,
                    const uint16_t *key_cache, const uint16_t *value_cache,
                    const int32_t *block_tables, const int32_t *context_lengths, double scale,
                    int64_t row, int t0, int t1, double *m_out, double *l_out,
                    double *acc_out) {
-  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages};
+  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages, layout};
   if (check_dims(&p)) return 1;
   if (row < 0 || row >= (int64_t)batch * query_heads) return 5;
   int b = (int)(row / query_heads);

@@ -48,6 +48,11 @@ pa_status_t check_problem(const pa_problem_t *p) {
     return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(p->batch) * p->query_heads * p->head_dim >= (int64_t(1) << 40))
     return PA_ERR_UNSUPPORTED;
+  if (p->cache_layout != PA_LAYOUT_TOKEN_MAJOR && p->cache_layout != PA_LAYOUT_HEAD_MAJOR)
+    return PA_ERR_INVALID_ARG;
+  if (p->cache_layout == PA_LAYOUT_HEAD_MAJOR &&
+      static_cast<int64_t>(p->num_physical_pages) * p->kv_heads >= (int64_t(1) << 31))
+    return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
@@ -227,17 +232,31 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D map over a cache viewed as [num_pages * page_size rows][kv_heads][head_dim] with a
-// box of (64 elements, 1 head, rows_per_box rows) and 128-byte swizzle.
+// 3-D map over a cache with a box of rows_per_box rows of one head, 64 elements wide, and
+// 128-byte swizzle. Token-major caches are viewed as [num_pages * page_size rows][kv_heads]
+// [head_dim] (box 64 x 1 x rows), head-major ones as [num_pages * kv_heads][page_size]
+// [head_dim] (box 64 x rows x 1); either way a box lands as rows x 128 bytes.
 pa_status_t encode_cache_map(CUtensorMap *map, const void *base, const pa_problem_t *p,
                              int rows_per_box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return PA_ERR_CUDA;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->head_dim), static_cast<cuuint64_t>(p->kv_heads),
-                        static_cast<cuuint64_t>(p->num_physical_pages) * p->page_size};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(p->head_dim) * 2,
-                           static_cast<cuuint64_t>(p->kv_heads) * p->head_dim * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows_per_box)};
+  const bool hm = p->cache_layout == PA_LAYOUT_HEAD_MAJOR;
+  const cuuint64_t hd = static_cast<cuuint64_t>(p->head_dim);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3] = {64, 1, 1};
+  dims[0] = hd;
+  strides[0] = hd * 2;
+  if (hm) {
+    dims[1] = static_cast<cuuint64_t>(p->page_size);
+    dims[2] = static_cast<cuuint64_t>(p->num_physical_pages) * p->kv_heads;
+    strides[1] = static_cast<cuuint64_t>(p->page_size) * hd * 2;
+    box[1] = static_cast<cuuint32_t>(rows_per_box);
+  } else {
+    dims[1] = static_cast<cuuint64_t>(p->kv_heads);
+    dims[2] = static_cast<cuuint64_t>(p->num_physical_pages) * p->page_size;
+    strides[1] = static_cast<cuuint64_t>(p->kv_heads) * hd * 2;
+    box[2] = static_cast<cuuint32_t>(rows_per_box);
+  }
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -321,6 +340,7 @@ void fill_args(KernelArgs *a, const pa_problem_t *p, const Resolved &r, const vo
   a->ps_shift = ilog2(p->page_size);
   a->maxp = p->max_pages_per_sequence;
   a->num_pages = p->num_physical_pages;
+  a->layout = p->cache_layout;
   a->g = r.g;
   a->sub = r.sub;
   a->nh_unit = r.nh_unit;

@@ -195,18 +195,28 @@ __device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMa
   const int pieces = T / R;
   const int kv = (c.us * a.group + member) / a.sub;
   const int npages = (c.end + a.ps - 1) >> a.ps_shift;
-  int row[kMaxPieces];
+  // TMA coordinates of each piece: token-major (y, z) = (kv, page * ps + slot),
+  // head-major (y, z) = (slot, page * kv_heads + kv); z < 0 marks a piece not loaded
+  int yc[kMaxPieces], zc[kMaxPieces];
   uint32_t bytes = 0;
 #pragma unroll
   for (int p = 0; p < kMaxPieces; ++p) {
-    row[p] = -1;
+    zc[p] = -1;
+    yc[p] = 0;
     const int tok = c.tok + p * R;
     if (p < pieces && tok < c.end) {
       const int page = bt_page(a, w, c.b, tok >> a.ps_shift, npages);
       if (page < 0 || page >= a.num_pages) {
         if ((threadIdx.x & 31) == 0) atomicOr(a.err, PA_DEVERR_PAGE_ID);
       } else {
-        row[p] = (page << a.ps_shift) + (tok & (a.ps - 1));
+        const int slot = tok & (a.ps - 1);
+        if (a.layout == PA_LAYOUT_HEAD_MAJOR) {
+          yc[p] = slot;
+          zc[p] = page * a.kvh + kv;
+        } else {
+          yc[p] = kv;
+          zc[p] = (page << a.ps_shift) + slot;
+        }
         bytes += static_cast<uint32_t>(R * HD * 4);
       }
     }
@@ -215,12 +225,12 @@ __device__ __forceinline__ void issue_tile(const KernelArgs &a, const CUtensorMa
     mbar_arrive_expect_tx(bar, bytes + extra_tx);
 #pragma unroll
     for (int p = 0; p < kMaxPieces; ++p) {
-      if (row[p] < 0) continue;
+      if (zc[p] < 0) continue;
 #pragma unroll
       for (int blk = 0; blk < HD / 64; ++blk) {
         const uint32_t dst = stage + blk * (T * 128) + p * R * 128;
-        tma_load_3d(dst, tk, bar, blk * 64, kv, row[p], pol);
-        tma_load_3d(dst + Geom<HD, T>::kHalfBytes, tv, bar, blk * 64, kv, row[p], pol);
+        tma_load_3d(dst, tk, bar, blk * 64, yc[p], zc[p], pol);
+        tma_load_3d(dst + Geom<HD, T>::kHalfBytes, tv, bar, blk * 64, yc[p], zc[p], pol);
       }
     }
   }

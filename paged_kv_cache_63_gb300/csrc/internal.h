@@ -42,6 +42,7 @@ struct KernelArgs {
   float *p_out;
   unsigned *err;  // device error word
   int batch, qh, kvh, hd, ps, ps_shift, maxp, num_pages;
+  int layout;   // pa_cache_layout_t
   int g;        // query heads per K/V head
   int sub;      // units per K/V head
   int nh_unit;  // heads per unit (ceil(g / sub))

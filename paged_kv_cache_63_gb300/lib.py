@@ -45,7 +45,7 @@ class pa_problem_t(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("query_heads", ctypes.c_int32),
                 ("kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("max_pages_per_sequence", ctypes.c_int32),
-                ("num_physical_pages", ctypes.c_int32)]
+                ("num_physical_pages", ctypes.c_int32), ("cache_layout", ctypes.c_int32)]
 
 
 class pa_options_t(ctypes.Structure):
@@ -107,15 +107,16 @@ def load(path: Optional[str] = None):
 
 # ------------------------------------------------------------------ marshalling helpers
 def problem(batch, query_heads, kv_heads, head_dim, page_size, max_pages_per_sequence,
-            num_physical_pages) -> pa_problem_t:
+            num_physical_pages, cache_layout=0) -> pa_problem_t:
     return pa_problem_t(batch, query_heads, kv_heads, head_dim, page_size,
-                        max_pages_per_sequence, num_physical_pages)
+                        max_pages_per_sequence, num_physical_pages, cache_layout)
 
 
 def problem_of(w) -> pa_problem_t:
     """pa_problem_t of a ``workloads.Workload`` (or any object with the same fields)."""
     return problem(w.batch, w.query_heads, w.kv_heads, w.head_dim, w.page_size,
-                   w.max_pages_per_sequence, w.num_physical_pages)
+                   w.max_pages_per_sequence, w.num_physical_pages,
+                   getattr(w, "cache_layout", 0))
 
 
 def options(schedule="auto", math="auto", combine="auto", workers=0, stages=0,

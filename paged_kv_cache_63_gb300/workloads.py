@@ -10,6 +10,7 @@ Layouts follow "[TIL] Optimizing paged attention" (retepy.com), section
 * ``query``           fp16 ``[batch][query_heads][head_dim]`` (one token per sequence)
 * ``key_cache``       fp16 ``[num_physical_pages][page_size][kv_heads][head_dim]``
 * ``value_cache``     same layout as ``key_cache``
+  (``to_head_major`` gives the alternative ``[page][kv_heads][page_size][head_dim]``)
 * ``block_tables``    int32 ``[batch][max_pages_per_sequence]``; entries past
   ``ceil(context_length / page_size)`` are placeholders, filled with -1 here
 * ``context_lengths`` int32 ``[batch]``
@@ -90,6 +91,7 @@ class Workload:
     value_cache: np.ndarray
     block_tables: np.ndarray
     context_lengths: np.ndarray
+    cache_layout: int = 0  # 0: [page][slot][kv_head][dim]; 1: [page][kv_head][slot][dim]
 
     @property
     def name(self) -> str:
@@ -105,6 +107,15 @@ class Workload:
         """Bytes of K and V that one decode step must read (each once)."""
         return int(self.context_lengths.astype(np.int64).clip(min=0).sum()) * \
             self.kv_heads * self.head_dim * 2 * 2
+
+
+def to_head_major(w: Workload) -> Workload:
+    """The same workload with both caches re-laid out as [page][kv_head][slot][head_dim]."""
+    if w.cache_layout == 1:
+        return w
+    k = np.ascontiguousarray(w.key_cache.transpose(0, 2, 1, 3))
+    v = np.ascontiguousarray(w.value_cache.transpose(0, 2, 1, 3))
+    return dataclasses.replace(w, key_cache=k, value_cache=v, cache_layout=1)
 
 
 def _draw_fp16(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:

@@ -24,15 +24,21 @@ from fractions import Fraction
 
 import numpy as np
 
-from paged_kv_cache_63_gb300.workloads import Workload, make_workload
+from paged_kv_cache_63_gb300.workloads import Workload, make_workload, to_head_major
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 # ---------------------------------------------------------------- helpers (no oracle code)
+def _kv_row(cache: np.ndarray, layout: int, page: int, slot: int, kv: int) -> np.ndarray:
+    """One head's row of a cache in either layout (0: [page][slot][kv]; 1: [page][kv][slot])."""
+    return cache[page, kv, slot] if layout == 1 else cache[page, slot, kv]
+
+
 def brute_force_row(w: Workload, b: int, h: int, scale=None):
     """Softmax attention of one (b, h) in plain Python with exactly rounded sums."""
     g = w.query_heads // w.kv_heads
+    lay = getattr(w, "cache_layout", 0)
     kv = h // g
     n = int(w.context_lengths[b])
     sc = float(w.scale if scale is None else scale)
@@ -41,15 +47,15 @@ def brute_force_row(w: Workload, b: int, h: int, scale=None):
     for t in range(n):
         page = int(w.block_tables[b, t // w.page_size])
         rows.append((page, t % w.page_size))
-    s = [sc * math.fsum(q[d] * float(w.key_cache[p, sl, kv, d]) for d in range(w.head_dim))
-         for p, sl in rows]
+    s = [sc * math.fsum(q[d] * float(_kv_row(w.key_cache, lay, p, sl, kv)[d])
+                        for d in range(w.head_dim)) for p, sl in rows]
     if n == 0:
         return [0.0] * w.head_dim, s
     m = max(s)
     wts = [math.exp(x - m) for x in s]
     L = math.fsum(wts)
-    out = [math.fsum(wts[t] * float(w.value_cache[p, sl, kv, d]) for t, (p, sl) in enumerate(rows))
-           / L for d in range(w.head_dim)]
+    out = [math.fsum(wts[t] * float(_kv_row(w.value_cache, lay, p, sl, kv)[d])
+                     for t, (p, sl) in enumerate(rows)) / L for d in range(w.head_dim)]
     return out, s
 
 
@@ -59,6 +65,8 @@ def gather_v(w: Workload, b: int, h: int) -> np.ndarray:
     n = int(w.context_lengths[b])
     t = np.arange(n)
     pages = w.block_tables[b, t // w.page_size]
+    if getattr(w, "cache_layout", 0) == 1:
+        return w.value_cache[pages, h // g, t % w.page_size].astype(np.float64)
     return w.value_cache[pages, t % w.page_size, h // g].astype(np.float64)
 
 
@@ -333,6 +341,22 @@ def pin_row_subset(o):
     full = o.decode(w).reshape(-1, w.head_dim)
     rows = [0, 5, 11, 7]
     assert np.array_equal(o.decode(w, rows=rows), full[rows])
+
+
+def pin_head_major_layout(o):
+    """The [page][kv_head][slot][head_dim] layout gives exactly the same results as the
+    pages' [page][slot][kv_head][head_dim] layout, and matches brute force."""
+    for w in (make_workload("tiny"), small("gqa4_mid", seed=8, context_lengths=[33, 1, 70],
+                                           head_dim=64, spare_pages=3)):
+        hm = to_head_major(w)
+        assert hm.key_cache.shape == (w.num_physical_pages, w.kv_heads, w.page_size, w.head_dim)
+        a = o.decode(w)
+        b = o.decode(hm)
+        assert np.array_equal(a, b)
+        for bb in range(w.batch):
+            for h in range(0, w.query_heads, 3):
+                ref, _ = brute_force_row(hm, bb, h)
+                _close(b[bb, h], ref)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -35,6 +35,9 @@ MUTANTS = {
     "merge_beta_missing": ("L = alpha * L + beta * l[i];", "L = alpha * L + l[i];"),
     "half_bias": ("v = ldexp((double)(f + 1024), e - 25);", "v = ldexp((double)(f + 1024), e - 24);"),
     "half_subnormal": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -14);"),
+    "head_major_swapped": (
+        "if (p->layout == 1) return ((page * p->kv_heads + kv) * (int64_t)p->page_size + slot) * p->head_dim;",
+        "if (p->layout == 1) return ((page * p->page_size + slot) * (int64_t)p->kv_heads + kv) * p->head_dim;"),
     "value_from_key": ("const uint16_t *vrow = value + cache_row", "const uint16_t *vrow = key + cache_row"),
 }
 

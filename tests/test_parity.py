@@ -130,3 +130,26 @@ def test_tile16_parity(name, opt):
     assert_close(got, ref, f"{name}/{opt}/t16")
     assert lib.status_of(lib.pa_plan, lib.problem_of(make_workload("long_gqa6")),
                          lib.options(tile_tokens=32)) == 2
+
+
+@pytest.mark.parametrize("opt", ["mma-single", "mma-balanced", "mma-balanced-kernel", "simt-balanced-w7"])
+@pytest.mark.parametrize("name", ["tiny", "mid_small", "long_small", "ragged_small", "g12",
+                                  "g3_hd64_ps8", "empty_ctx"])
+def test_head_major_parity(name, opt):
+    """The [page][kv_head][slot][head_dim] cache layout (the oracle gives the same result for
+    both layouts, exactly)."""
+    from paged_kv_cache_63_gb300.workloads import to_head_major
+
+    w, ref = case(name)
+    assert_close(run(to_head_major(w), opts=lib.options(**OPTS[opt])), ref, f"{name}/{opt}/hm")
+
+
+@pytest.mark.parametrize("name", ["gqa4_mid", "mha"])
+def test_head_major_full_size_sampled(name):
+    import oracle
+    from paged_kv_cache_63_gb300.workloads import to_head_major
+
+    w = to_head_major(make_workload(name))
+    got = run(w).reshape(-1, w.head_dim)
+    rows = sorted(np.random.default_rng(5).choice(w.batch * w.query_heads, 24, replace=False))
+    assert_close(got[rows], oracle.decode(w, rows=rows), name)

@@ -31,11 +31,17 @@ def poisoned(w):
     return dataclasses.replace(w, key_cache=k, value_cache=v)
 
 
+@pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("opt", sorted(OPTS))
-def test_poisoned_slots_are_never_read(opt):
+def test_poisoned_slots_are_never_read(opt, layout):
+    from paged_kv_cache_63_gb300.workloads import to_head_major
+
     w = make_workload("gqa4_mid", context_lengths=[5, 17, 33, 250, 0, 1], spare_pages=3)
+    bad = poisoned(w)
+    if layout:
+        w, bad = to_head_major(w), to_head_major(bad)
     clean = run(w, opts=lib.options(**OPTS[opt]))
-    dirty = run(poisoned(w), opts=lib.options(**OPTS[opt]))
+    dirty = run(bad, opts=lib.options(**OPTS[opt]))
     assert np.isfinite(dirty).all()
     assert np.array_equal(clean, dirty)
 
