@@ -243,6 +243,20 @@ pa_status_t pa_split_kv_combine(const pa_problem_t *problem, int32_t num_splits,
                                 const float *partial_max, const float *partial_sum,
                                 const float *partial_out, float *out, void *stream);
 
+/* Append one token per sequence to the paged caches: new_key[b][h][:] and new_value[b][h]
+ * [:] (fp16, [batch][kv_heads][head_dim], 16-byte aligned) are written at token index
+ * t = context_lengths[b] -- physical page block_tables[b][t / page_size], slot t % page_size,
+ * in the problem's cache_layout. This is the cache write that precedes a decode step ("[TIL]
+ * Optimizing paged attention", section "Paged Attention": the K and V of earlier tokens are
+ * kept and reused); context_lengths holds the lengths before the append, and the caller
+ * decodes with each length plus one afterwards. The page for index t must already be in
+ * the block table. A sequence whose t is outside [0, max_pages_per_sequence * page_size) or
+ * whose page id is outside the pool is skipped and flagged (PA_DEVERR_CONTEXT /
+ * PA_DEVERR_PAGE_ID). Two sequences appending to the same (page, slot) race. */
+pa_status_t pa_append_kv(const pa_problem_t *problem, const void *new_key, const void *new_value,
+                         const int32_t *block_tables, const int32_t *context_lengths,
+                         void *key_cache, void *value_cache, void *stream);
+
 /* Read and clear the device error word of the current device (PA_DEVERR_* bits) after
  * the work queued on `stream` finishes. Synchronises `stream`. */
 pa_status_t pa_get_device_error(void *stream, uint32_t *flags);

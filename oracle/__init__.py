@@ -10,6 +10,7 @@ attention", sections "Data Layout", "Baseline" and "V4 (Context-axis parallelism
 * ``decode``  -- softmax(scale * q K^T) V per (sequence, query head), two-pass, fp64
 * ``partial`` -- the (max, sum, unnormalised accumulator) state of one token range
 * ``combine`` -- log-sum-exp merge of such states
+* ``append_kv`` -- the cache write of one new token per sequence
 * ``half_to_double`` -- the exact binary16 widening the oracle uses
 """
 
@@ -61,6 +62,8 @@ def _bind(path: str):
                                                        i32, p, p, p]
     lib.oracle_combine.restype = None
     lib.oracle_combine.argtypes = [i32, i32, p, p, p, p]
+    lib.oracle_append_kv.restype = i32
+    lib.oracle_append_kv.argtypes = [i32] * 8 + [p] * 6
     lib.oracle_max_threads.restype = i32
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -135,6 +138,20 @@ class Oracle:
             raise ValueError(f"oracle_partial rejected the inputs (code {rc})")
         return float(m[0]), float(l[0]), acc
 
+    def append_kv(self, w, new_key, new_value):
+        """Caches after appending new_key/new_value ([batch][kv_heads][head_dim] fp16) at
+        token index context_lengths[b]; returns (key_cache, value_cache, flags)."""
+        lib = self._lib
+        dims, q, k, v, bt, ctx = _inputs(w)
+        k = k.copy()
+        v = v.copy()
+        nk = np.ascontiguousarray(new_key, dtype=np.float16).view(np.uint16)
+        nv = np.ascontiguousarray(new_value, dtype=np.float16).view(np.uint16)
+        rc = lib.oracle_append_kv(*dims, _ptr(nk), _ptr(nv), _ptr(bt), _ptr(ctx), _ptr(k), _ptr(v))
+        if rc < 0:
+            raise ValueError("oracle_append_kv rejected the dimensions")
+        return k.view(np.float16), v.view(np.float16), int(rc)
+
     def combine(self, m, l, acc) -> np.ndarray:
         """Log-sum-exp merge of states m[n], l[n], acc[n, head_dim] -> normalised row."""
         lib = self._lib
@@ -177,3 +194,7 @@ def partial(w, row: int, t0: int, t1: int, scale=None):
 
 def combine(m, l, acc) -> np.ndarray:
     return _oracle().combine(m, l, acc)
+
+
+def append_kv(w, new_key, new_value):
+    return _oracle().append_kv(w, new_key, new_value)

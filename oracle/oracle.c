@@ -235,6 +235,44 @@ void oracle_combine(int n, int head_dim, const double *m, const double *l, const
   for (int d = 0; d < head_dim; ++d) out[d] /= L;
 }
 
+/* Append one token per sequence: the new K and V rows (fp16 bits, [batch][kv_heads]
+ * [head_dim]) are written at token index t = context_lengths[b], i.e. physical page
+ * block_tables[b][t / page_size], slot t % page_size, in the given layout -- the cache write
+ * that precedes a decode step ("[TIL] Optimizing paged attention", section "Paged Attention":
+ * the K and V of earlier tokens are kept and reused). A sequence whose t is outside
+ * [0, max_pages * page_size) or whose page id is outside the pool is skipped; the return
+ * value has bit 1 set for a page id and bit 2 for a length (0 if all rows were written). */
+int oracle_append_kv(int batch, int query_heads, int kv_heads, int head_dim, int page_size,
+                     int max_pages, int num_pages, int layout, const uint16_t *new_key,
+                     const uint16_t *new_value, const int32_t *block_tables,
+                     const int32_t *context_lengths, uint16_t *key_cache,
+                     uint16_t *value_cache) {
+  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages, layout};
+  if (check_dims(&p)) return -1;
+  int flags = 0;
+  for (int b = 0; b < batch; ++b) {
+    int t = context_lengths[b];
+    if (t < 0 || (int64_t)t >= (int64_t)max_pages * page_size) {
+      flags |= 2;
+      continue;
+    }
+    int page = block_tables[(int64_t)b * max_pages + t / page_size];
+    if (page < 0 || page >= num_pages) {
+      flags |= 1;
+      continue;
+    }
+    for (int kv = 0; kv < kv_heads; ++kv) {
+      int64_t dst = cache_row(&p, page, t % page_size, kv);
+      int64_t src = ((int64_t)b * kv_heads + kv) * head_dim;
+      for (int d = 0; d < head_dim; ++d) {
+        key_cache[dst + d] = new_key[src + d];
+        value_cache[dst + d] = new_value[src + d];
+      }
+    }
+  }
+  return flags;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

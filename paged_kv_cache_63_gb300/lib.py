@@ -30,7 +30,7 @@ COMBINE = {"auto": 0, "fused": 1, "kernel": 2}
 
 # Every entry point include/pagedattn.h declares.
 EXPORTS = ("pa_plan", "pa_workspace_size", "pa_workspace_init", "pa_decode", "pa_decode_ex",
-           "pa_decode_noalloc",
+           "pa_decode_noalloc", "pa_append_kv",
            "pa_split_kv_partial", "pa_split_kv_combine", "pa_get_device_error",
            "pa_status_string", "pa_version")
 
@@ -90,6 +90,7 @@ def load(path: Optional[str] = None):
         lib.pa_decode_ex.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, P(pa_options_t),
                                      vp, ctypes.c_size_t, vp]
         lib.pa_decode_noalloc.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, vp]
+        lib.pa_append_kv.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, vp, vp]
         lib.pa_split_kv_partial.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, i32, i32, vp,
                                             vp, vp, vp]
         lib.pa_split_kv_combine.argtypes = [P(pa_problem_t), i32, vp, vp, vp, vp, vp]
@@ -206,6 +207,14 @@ def pa_decode_noalloc(prob, query, key_cache, value_cache, block_tables, context
 
 
 PA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def pa_append_kv(prob, new_key, new_value, block_tables, context_lengths, key_cache, value_cache,
+                 stream=None):
+    """Write one new K/V row per (sequence, K/V head) at token index context_lengths[b]."""
+    _check(load().pa_append_kv(ctypes.byref(prob), _ptr(new_key), _ptr(new_value),
+                               _ptr(block_tables), _ptr(context_lengths), _ptr(key_cache),
+                               _ptr(value_cache), _stream(stream)), "pa_append_kv")
 
 
 def pa_split_kv_partial(prob, query, key_cache, value_cache, block_tables, context_lengths, scale,

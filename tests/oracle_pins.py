@@ -359,4 +359,86 @@ def pin_head_major_layout(o):
                 _close(b[bb, h], ref)
 
 
+def _new_rows(w, seed=3):
+    rng = np.random.default_rng(seed)
+    shape = (w.batch, w.kv_heads, w.head_dim)
+    return (rng.standard_normal(shape).astype(np.float16),
+            rng.standard_normal(shape).astype(np.float16))
+
+
+def pin_append_places_row(o):
+    """Append writes sequence b's new rows at page block_tables[b][t / ps], slot t % ps
+    (t = its length) in either layout, and changes nothing else."""
+    for layout in (0, 1):
+        w = small("tiny", context_lengths=[5, 16, 31], spare_pages=2)
+        w = replace(w, block_tables=w.block_tables.copy())
+        # sequence 1 fills its page exactly: its next token needs a fresh page
+        w.block_tables[1, 1] = w.num_physical_pages - 1
+        if layout:
+            w = to_head_major(w)
+        nk, nv = _new_rows(w)
+        k, v, flags = o.append_kv(w, nk, nv)
+        assert flags == 0
+        ek = w.key_cache.copy()
+        ev = w.value_cache.copy()
+        for b in range(w.batch):
+            t = int(w.context_lengths[b])
+            page, slot = int(w.block_tables[b, t // w.page_size]), t % w.page_size
+            for kv in range(w.kv_heads):
+                if layout:
+                    ek[page, kv, slot] = nk[b, kv]
+                    ev[page, kv, slot] = nv[b, kv]
+                else:
+                    ek[page, slot, kv] = nk[b, kv]
+                    ev[page, slot, kv] = nv[b, kv]
+        assert np.array_equal(k.view(np.uint16), ek.view(np.uint16))
+        assert np.array_equal(v.view(np.uint16), ev.view(np.uint16))
+
+
+def pin_append_then_decode(o):
+    """Decoding with length t + 1 after appending equals brute force over the extended
+    sequence (the appended row is the last token)."""
+    w = small("tiny", context_lengths=[7, 40])
+    nk, nv = _new_rows(w, seed=9)
+    k, v, _ = o.append_kv(w, nk, nv)
+    w2 = replace(w, key_cache=k, value_cache=v, context_lengths=w.context_lengths + 1)
+    out = o.decode(w2)
+    for b in range(w.batch):
+        for h in range(w.query_heads):
+            ref, _ = brute_force_row(w2, b, h)
+            _close(out[b, h], ref)
+            # the appended token's row is what brute force read last
+            g = w.query_heads // w.kv_heads
+            assert np.array_equal(gather_v(w2, b, h)[-1], nv[b, h // g].astype(np.float64))
+
+
+def pin_append_golden_sketch(o):
+    """The pages' block-table sketch: stream 3 (5 tokens, pages 16 17 18, page size 2) appends
+    its 6th token at page 18, slot 1; a full stream (6 tokens, 3 of 8 pages) needs its 4th
+    table entry, a placeholder, so it is refused, not written."""
+    d = load_golden("block_table_sketch.json")
+    w = _golden_workload(d, poison_nan=False)
+    nk = np.full((w.batch, w.kv_heads, w.head_dim), 7.0, dtype=np.float16)
+    nv = np.full((w.batch, w.kv_heads, w.head_dim), -3.0, dtype=np.float16)
+    k, v, flags = o.append_kv(w, nk, nv)
+    assert flags == 1  # streams 1 and 2 hit the placeholder entry -1
+    assert (v[18, 1, 0] == -3.0).all() and (k[18, 1, 0] == 7.0).all()
+    changed = np.argwhere((v.view(np.uint16) != w.value_cache.view(np.uint16)).any(axis=(2, 3)))
+    assert [tuple(x) for x in changed] == [(18, 1)]
+
+
+def pin_append_rejects_bad_indices(o):
+    """A length at the table's capacity or a page outside the pool is skipped and flagged."""
+    w = small("tiny", context_lengths=[3, 9])
+    ctx = w.context_lengths.copy()
+    ctx[0] = w.max_pages_per_sequence * w.page_size
+    nk, nv = _new_rows(w)
+    k, v, flags = o.append_kv(replace(w, context_lengths=ctx), nk, nv)
+    assert flags & 2
+    bt = w.block_tables.copy()
+    bt[1, 0] = w.num_physical_pages
+    k2, v2, flags2 = o.append_kv(replace(w, block_tables=bt), nk, nv)
+    assert flags2 & 1
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -60,7 +60,7 @@ def P(**kw):
     (dict(num_physical_pages=1 << 27), 2),
     (dict(max_pages_per_sequence=0), 1),
     (dict(cache_layout=2), 1),
-    (dict(cache_layout=1, num_physical_pages=1 << 27, page_size=8), 2),
+    (dict(cache_layout=1, num_physical_pages=1 << 27, page_size=8, kv_heads=16), 2),
 ])
 def test_plan_rejects_bad_problems(kw, status):
     assert lib.status_of(lib.pa_plan, P(**kw)) == status

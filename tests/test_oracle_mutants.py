@@ -38,6 +38,10 @@ MUTANTS = {
     "head_major_swapped": (
         "if (p->layout == 1) return ((page * p->kv_heads + kv) * (int64_t)p->page_size + slot) * p->head_dim;",
         "if (p->layout == 1) return ((page * p->page_size + slot) * (int64_t)p->kv_heads + kv) * p->head_dim;"),
+    "append_slot_off": ("int64_t dst = cache_row(&p, page, t % page_size, kv);",
+                        "int64_t dst = cache_row(&p, page, (t + 1) % page_size, kv);"),
+    "append_src_transposed": ("int64_t src = ((int64_t)b * kv_heads + kv) * head_dim;",
+                              "int64_t src = ((int64_t)kv * batch + b) * head_dim;"),
     "value_from_key": ("const uint16_t *vrow = value + cache_row", "const uint16_t *vrow = key + cache_row"),
 }
 
