@@ -234,6 +234,18 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
     return ms, wall, clocks
 
 
+def reduce_over_ranks(torch, device, maxima, sums):
+    """Whole-job figures for weak scaling: the slowest rank's times (max over ranks) and the
+    bytes all ranks moved (sum). With one process the values pass through."""
+    t_max = torch.tensor([float(x) for x in maxima], dtype=torch.float64, device=device)
+    t_sum = torch.tensor([float(x) for x in sums], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized() and \
+            torch.distributed.get_world_size() > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(t_sum, op=torch.distributed.ReduceOp.SUM)
+    return t_max.tolist(), t_sum.tolist()
+
+
 def cpu_baseline(w, seconds: float) -> dict:
     """The fp64 oracle on the host cores over a bounded sample of the same workload: all
     query heads of a subset of sequences (calibrated to about `seconds` of work)."""
@@ -302,25 +314,23 @@ def run_ours(args):
     ms, wall, clocks = time_decode(w, d, opts, args.steps, args.warmup, torch, lib,
                                    sampler_dev=smi_index if rank == 0 else None)
     assert lib.pa_get_device_error() == 0
-    t = torch.tensor([sum(ms) / len(ms)], dtype=torch.float64, device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_step = float(t.item())
     e2e_ms, _, _ = time_decode(w, d, opts, max(10, args.steps // 4), args.warmup, torch, lib,
                                e2e=True)
-    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    (ms_step, e2e_step), (kv_all, total_all) = reduce_over_ranks(
+        torch, "cuda", [sum(ms) / len(ms), sum(e2e_ms) / len(e2e_ms)],
+        [nbytes["kv"], nbytes["total"]])
     if rank != 0:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
         return
     peak, peak_kind = measured_peak()
-    achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9
+    achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9  # this GPU's kernel (rank 0)
     kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
     launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 2) else 1
     traffic = recorded_traffic(w.name)
     line = {
         "metric": METRIC,
-        "value": round(kv_gbs * world, 2),
+        "value": round(kv_all / (ms_step * 1e-3) / 1e9, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -341,7 +351,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": nbytes["total"],
                      "kernel": "pa::decode_kernel"},
         "clocks": clocks,
-        "e2e": {"value": round(nbytes["kv"] / (e2e_step * 1e-3) / 1e9 * world, 2), "unit": "GB/s",
+        "e2e": {"value": round(kv_all / (e2e_step * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_call": round(e2e_step * 1e3, 2),
                 "h2d_bytes_per_step": nbytes["h2d"], "d2h_bytes_per_step": nbytes["d2h"],
                 "note": "q, block tables and context lengths copied every step from one pinned host "
