@@ -11,6 +11,7 @@ attention", sections "Data Layout", "Baseline" and "V4 (Context-axis parallelism
 * ``partial`` -- the (max, sum, unnormalised accumulator) state of one token range
 * ``combine`` -- log-sum-exp merge of such states
 * ``append_kv`` -- the cache write of one new token per sequence
+* ``prefill`` -- causal attention of several new tokens per sequence
 * ``half_to_double`` -- the exact binary16 widening the oracle uses
 """
 
@@ -62,6 +63,8 @@ def _bind(path: str):
                                                        i32, p, p, p]
     lib.oracle_combine.restype = None
     lib.oracle_combine.argtypes = [i32, i32, p, p, p, p]
+    lib.oracle_prefill.restype = i32
+    lib.oracle_prefill.argtypes = [i32] * 8 + [p] * 6 + [ctypes.c_double, p, ctypes.c_int64, p, i32]
     lib.oracle_append_kv.restype = i32
     lib.oracle_append_kv.argtypes = [i32] * 8 + [p] * 6
     lib.oracle_max_threads.restype = i32
@@ -138,6 +141,29 @@ class Oracle:
             raise ValueError(f"oracle_partial rejected the inputs (code {rc})")
         return float(m[0]), float(l[0]), acc
 
+    def prefill(self, w, query, query_start, rows=None, scale=None, threads: int = 0):
+        """Causal multi-token attention: query [total][qh][hd] fp16 holds each sequence's
+        last n_b tokens (n_b = query_start[b+1] - query_start[b]). fp64 output [total][qh][hd]
+        (or the listed flat rows i * qh + h)."""
+        lib = self._lib
+        dims, _, k, v, bt, ctx = _inputs(w)
+        qq = np.ascontiguousarray(query, dtype=np.float16).view(np.uint16)
+        qs = np.ascontiguousarray(query_start, dtype=np.int32)
+        s = float(w.scale if scale is None else scale)
+        total = int(qs[-1])
+        if rows is None:
+            out = np.zeros((total, w.query_heads, w.head_dim))
+            rc = lib.oracle_prefill(*dims, _ptr(qq), _ptr(qs), _ptr(k), _ptr(v), _ptr(bt), _ptr(ctx),
+                                    s, None, 0, _ptr(out), int(threads))
+        else:
+            r = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1)
+            out = np.zeros((r.size, w.head_dim))
+            rc = lib.oracle_prefill(*dims, _ptr(qq), _ptr(qs), _ptr(k), _ptr(v), _ptr(bt), _ptr(ctx),
+                                    s, _ptr(r), int(r.size), _ptr(out), int(threads))
+        if rc:
+            raise ValueError(f"oracle_prefill rejected the inputs (code {rc})")
+        return out
+
     def append_kv(self, w, new_key, new_value):
         """Caches after appending new_key/new_value ([batch][kv_heads][head_dim] fp16) at
         token index context_lengths[b]; returns (key_cache, value_cache, flags)."""
@@ -198,3 +224,7 @@ def combine(m, l, acc) -> np.ndarray:
 
 def append_kv(w, new_key, new_value):
     return _oracle().append_kv(w, new_key, new_value)
+
+
+def prefill(w, query, query_start, rows=None, scale=None, threads: int = 0):
+    return _oracle().prefill(w, query, query_start, rows=rows, scale=scale, threads=threads)

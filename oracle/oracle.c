@@ -63,11 +63,10 @@ static int64_t cache_row(const dims_t *p, int64_t page, int slot, int kv) {
 
 /* Scores s_t = scale * q . K_t for t in [t0, t1) of one (sequence, q head). Returns 0 on
  * success, 2 on an out-of-range page id. */
-static int scores(const dims_t *p, const uint16_t *q, const uint16_t *key, const int32_t *bt,
-                  int b, int h, double scale, int t0, int t1, double *s) {
+static int scores(const dims_t *p, const uint16_t *qrow, const uint16_t *key,
+                  const int32_t *bt, int b, int h, double scale, int t0, int t1, double *s) {
   int g = p->query_heads / p->kv_heads;
   int kv = h / g;
-  const uint16_t *qrow = q + ((int64_t)b * p->query_heads + h) * p->head_dim;
   for (int t = t0; t < t1; ++t) {
     int lp = t / p->page_size;
     int slot = t % p->page_size;
@@ -91,20 +90,18 @@ static int check_dims(const dims_t *p) {
   return 0;
 }
 
-/* One output row: out[d] = sum_t w_t V_t[d] / sum_t w_t with w_t = exp(s_t - max s). */
-static int decode_row(const dims_t *p, const uint16_t *q, const uint16_t *key,
-                      const uint16_t *value, const int32_t *bt, const int32_t *ctx,
-                      double scale, int64_t row, double *out) {
-  int b = (int)(row / p->query_heads);
-  int h = (int)(row % p->query_heads);
-  int n = ctx[b];
+/* Attention of query vector qrow (query head h of sequence b) over tokens [0, n):
+ * out[d] = sum_t w_t V_t[d] / sum_t w_t with w_t = exp(s_t - max s). */
+static int attend(const dims_t *p, const uint16_t *qrow, const uint16_t *key,
+                  const uint16_t *value, const int32_t *bt, int b, int h, int n, double scale,
+                  double *out) {
   int hd = p->head_dim;
   for (int d = 0; d < hd; ++d) out[d] = 0.0;
   if (n < 0 || (int64_t)n > (int64_t)p->max_pages * p->page_size) return 3;
   if (n == 0) return 0;
   double *s = (double *)malloc(sizeof(double) * (size_t)n);
   if (!s) return 4;
-  int rc = scores(p, q, key, bt, b, h, scale, 0, n, s);
+  int rc = scores(p, qrow, key, bt, b, h, scale, 0, n, s);
   if (rc) {
     free(s);
     return rc;
@@ -129,6 +126,15 @@ static int decode_row(const dims_t *p, const uint16_t *q, const uint16_t *key,
   return 0;
 }
 
+/* One decode output row: the sequence's single query token attends to all ctx[b] tokens. */
+static int decode_row(const dims_t *p, const uint16_t *q, const uint16_t *key,
+                      const uint16_t *value, const int32_t *bt, const int32_t *ctx,
+                      double scale, int64_t row, double *out) {
+  int b = (int)(row / p->query_heads);
+  int h = (int)(row % p->query_heads);
+  return attend(p, q + row * p->head_dim, key, value, bt, b, h, ctx[b], scale, out);
+}
+
 /* Full decode (rows == NULL: every (b, h), out is [batch][query_heads][head_dim]) or the
  * listed rows r = b * query_heads + h (out is [n_rows][head_dim]). n_threads <= 0 uses
  * the OpenMP default. Returns 0, or the first nonzero row code. */
@@ -151,6 +157,58 @@ int oracle_decode(int batch, int query_heads, int kv_heads, int head_dim, int pa
     if (r >= 0 && r < (int64_t)batch * query_heads)
       rc = decode_row(&p, query, key_cache, value_cache, block_tables, context_lengths, scale,
                       r, out + i * head_dim);
+    if (rc) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      if (!status) status = rc;
+    }
+  }
+  (void)n_threads;
+  return status;
+}
+
+/* Multi-token (prefill) attention: sequence b has n_b = query_start[b + 1] - query_start[b]
+ * new query tokens (rows query_start[b] .. of query, [total][query_heads][head_dim]); they
+ * are the last n_b of its context_lengths[b] tokens, so new token j sits at position
+ * p = context_lengths[b] - n_b + j and attends causally to tokens 0..p (the causal
+ * extension of the decode step: "[TIL] Optimizing paged attention", section "Paged
+ * Attention", applied to every new token). rows == NULL computes every (query row, head)
+ * into out [total][query_heads][head_dim]; otherwise the listed flat rows i * qh + h.
+ * Returns 0, 6 for inconsistent query_start / lengths, or a row code as decode. */
+int oracle_prefill(int batch, int query_heads, int kv_heads, int head_dim, int page_size,
+                   int max_pages, int num_pages, int layout, const uint16_t *query,
+                   const int32_t *query_start, const uint16_t *key_cache,
+                   const uint16_t *value_cache, const int32_t *block_tables,
+                   const int32_t *context_lengths, double scale, const int64_t *rows,
+                   int64_t n_rows, double *out, int n_threads) {
+  dims_t p = {batch, query_heads, kv_heads, head_dim, page_size, max_pages, num_pages, layout};
+  if (check_dims(&p)) return 1;
+  if (query_start[0] != 0) return 6;
+  for (int b = 0; b < batch; ++b) {
+    int nb = query_start[b + 1] - query_start[b];
+    if (nb < 0 || nb > context_lengths[b]) return 6;
+  }
+  const int64_t total = (int64_t)query_start[batch] * query_heads;
+  const int64_t count = rows ? n_rows : total;
+  int status = 0;
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t i = 0; i < count; ++i) {
+    int64_t r = rows ? rows[i] : i;
+    int rc = 5;
+    if (r >= 0 && r < total) {
+      int qi = (int)(r / query_heads);
+      int h = (int)(r % query_heads);
+      int b = 0;
+      while (query_start[b + 1] <= qi) ++b;
+      int nb = query_start[b + 1] - query_start[b];
+      int pos = context_lengths[b] - nb + (qi - query_start[b]);
+      rc = attend(&p, query + r * head_dim, key_cache, value_cache, block_tables, b, h, pos + 1,
+                  scale, out + i * head_dim);
+    }
     if (rc) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -187,7 +245,7 @@ int oracle_partial(int batch, int query_heads, int kv_heads, int head_dim, int p
   if (t1 <= t0) return 0;
   double *s = (double *)malloc(sizeof(double) * (size_t)(t1 - t0));
   if (!s) return 4;
-  int rc = scores(&p, query, key_cache, block_tables, b, h, scale, t0, t1, s);
+  int rc = scores(&p, query + row * head_dim, key_cache, block_tables, b, h, scale, t0, t1, s);
   if (rc) {
     free(s);
     return rc;

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for paged decode attention.
+"""Seeded synthetic inputs for paged decode attention and its multi-token variant.
 
 This module only draws random numbers and lays them out; it holds none of the
 attention arithmetic, so both the CUDA path and the CPU oracle can consume its
@@ -148,6 +148,75 @@ def _context_lengths(spec: Spec, rng: np.random.Generator, batch: int) -> np.nda
         x[ones] = 1
         return x
     raise ValueError(f"unknown context recipe {kind!r}")
+
+
+# Multi-token (prefill) workloads: the cache workload they extend and how many of each
+# sequence's tokens are new. ("all",) makes every token new (a fresh prompt);
+# ("last", n) makes the last min(n, ctx) tokens new (a prompt chunk appended to a
+# cached prefix).
+PREFILL_SPECS: Dict[str, tuple] = {
+    "prefill_tiny": ("tiny", dict(), ("fixed", [37, 20])),
+    "prefill_gqa4": ("gqa4_mid", dict(batch=8, context_lengths=[2048] * 8), ("all",)),
+    "prefill_chunked": ("gqa4_mid", dict(batch=16), ("last", 512)),
+    "prefill_mha": ("mha", dict(batch=8, context_lengths=[2048] * 8), ("all",)),
+}
+
+
+@dataclasses.dataclass
+class Prefill:
+    """A paged cache that already holds every sequence's tokens, plus the queries of the
+    last ``n_b`` tokens of sequence b: ``query`` fp16 ``[total][query_heads][head_dim]``,
+    rows ``query_start[b] .. query_start[b + 1]`` belong to sequence b."""
+
+    cache: Workload
+    query: np.ndarray
+    query_start: np.ndarray
+
+    @property
+    def new_tokens(self) -> np.ndarray:
+        return np.diff(self.query_start).astype(np.int32)
+
+    @property
+    def total(self) -> int:
+        return int(self.query_start[-1])
+
+    def max_query_len(self) -> int:
+        return int(self.new_tokens.max()) if self.cache.batch else 0
+
+    def causal_pairs(self) -> int:
+        """Number of (query token, attended token) pairs, per query head."""
+        ctx = self.cache.context_lengths.astype(np.int64)
+        n = self.new_tokens.astype(np.int64)
+        # new token j of sequence b attends to ctx - n + j + 1 tokens
+        return int((n * (ctx - n) + n * (n + 1) // 2).sum())
+
+
+def make_prefill(name: str, seed: Optional[int] = None, *, new_tokens=None, **cache_kw) -> Prefill:
+    """Build one seeded multi-token workload. ``new_tokens`` (one count per sequence) and
+    ``cache_kw`` (passed to ``make_workload``) reshape it for tests. The queries are drawn
+    after the cache, from a generator seeded with ``seed + 1000``."""
+    base, kw, recipe = PREFILL_SPECS[name]
+    kw = dict(kw)
+    kw.update(cache_kw)
+    w = make_workload(base, seed=seed, **kw)
+    ctx = w.context_lengths.astype(np.int64)
+    if new_tokens is not None:
+        n = np.asarray(new_tokens, dtype=np.int64).reshape(-1)
+    elif recipe[0] == "all":
+        n = ctx.copy()
+    elif recipe[0] == "last":
+        n = np.minimum(ctx, recipe[1])
+    elif recipe[0] == "fixed":
+        n = np.asarray(recipe[1], dtype=np.int64)
+    else:
+        raise ValueError(f"unknown new-token recipe {recipe[0]!r}")
+    if n.size != w.batch or (n < 0).any() or (n > ctx).any():
+        raise ValueError("new-token counts must be one per sequence, within [0, context length]")
+    qs = np.zeros(w.batch + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(n)
+    rng = np.random.default_rng((w.spec.seed if seed is None else seed) + 1000)
+    q = _draw_fp16(rng, (int(qs[-1]), w.query_heads, w.head_dim))
+    return Prefill(cache=w, query=q, query_start=qs)
 
 
 def make_workload(name: str, seed: Optional[int] = None, *, batch: Optional[int] = None,

@@ -441,4 +441,102 @@ def pin_append_rejects_bad_indices(o):
     assert flags2 & 1
 
 
+# ---------------------------------------------------------------- multi-token (prefill) pins
+def _prefill_small(seed=21, new_tokens=(5, 40, 0, 17), ctx=(5, 70, 9, 17)):
+    from paged_kv_cache_63_gb300.workloads import make_prefill
+    return make_prefill("prefill_chunked", seed=seed, new_tokens=list(new_tokens),
+                        context_lengths=list(ctx), max_pages_per_sequence=6, spare_pages=3,
+                        head_dim=64)
+
+
+def pin_prefill_one_token_is_decode(o):
+    """One new token per sequence is exactly the decode step (same query, whole context)."""
+    w = small("gqa4_mid", seed=7, context_lengths=[1, 17, 40], max_pages_per_sequence=4,
+              head_dim=64)
+    qs = np.arange(w.batch + 1, dtype=np.int32)
+    got = o.prefill(w, w.query, qs)
+    assert np.array_equal(got, o.decode(w))
+
+
+def pin_prefill_brute_force(o):
+    """Every (new token, head) row equals brute force over tokens 0..position, the position
+    being context_length - new_tokens + j for the j-th new token."""
+    p = _prefill_small()
+    w = p.cache
+    out = o.prefill(w, p.query, p.query_start)
+    for b in range(w.batch):
+        n = int(p.query_start[b + 1] - p.query_start[b])
+        for j in range(n):
+            i = int(p.query_start[b]) + j
+            pos = int(w.context_lengths[b]) - n + j
+            q = w.query.copy()
+            q[b] = p.query[i]
+            ctx = w.context_lengths.copy()
+            ctx[b] = pos + 1
+            wb = replace(w, query=q, context_lengths=ctx)
+            for h in range(w.query_heads):
+                ref, _ = brute_force_row(wb, b, h)
+                _close(out[i, h], ref)
+
+
+def pin_prefill_first_token_sees_itself(o):
+    """In a fresh prompt (every token new) the first token attends only to itself, so its
+    output is exactly its own V row (softmax over one score is 1)."""
+    p = _prefill_small(seed=23, new_tokens=(5, 70, 9, 17))
+    w = p.cache
+    out = o.prefill(w, p.query, p.query_start)
+    g = w.query_heads // w.kv_heads
+    for b in range(w.batch):
+        page = int(w.block_tables[b, 0])
+        for h in range(w.query_heads):
+            v0 = w.value_cache[page, 0, h // g].astype(np.float64)
+            assert np.array_equal(out[int(p.query_start[b]), h], v0)
+
+
+def pin_prefill_causal(o):
+    """Changing the K and V of each sequence's last token changes only the last new token's
+    rows; every earlier token's output is bit-for-bit unchanged."""
+    p = _prefill_small(seed=25)
+    w = p.cache
+    base = o.prefill(w, p.query, p.query_start)
+    k = w.key_cache.copy()
+    v = w.value_cache.copy()
+    last_rows = []
+    for b in range(w.batch):
+        n = int(p.query_start[b + 1] - p.query_start[b])
+        t = int(w.context_lengths[b]) - 1
+        if n == 0:
+            continue
+        page, slot = int(w.block_tables[b, t // w.page_size]), t % w.page_size
+        k[page, slot] = np.float16(3.0)
+        v[page, slot] = np.float16(-5.0)
+        last_rows.append(int(p.query_start[b + 1]) - 1)
+    got = o.prefill(replace(w, key_cache=k, value_cache=v), p.query, p.query_start)
+    keep = np.ones(p.total, dtype=bool)
+    keep[last_rows] = False
+    assert np.array_equal(got[keep], base[keep])
+    assert all(not np.array_equal(got[r], base[r]) for r in last_rows)
+
+
+def pin_prefill_rejects_bad_starts(o):
+    """More new tokens than context, or a start offset that is not 0, is refused."""
+    p = _prefill_small(seed=27)
+    w = p.cache
+    qs = p.query_start.copy()
+    qs[1:] += 1  # sequence 0 now claims ctx + 1 new tokens
+    try:
+        o.prefill(w, np.zeros((int(qs[-1]), w.query_heads, w.head_dim), np.float16), qs)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("accepted more new tokens than context")
+    qs2 = p.query_start + 1
+    try:
+        o.prefill(w, np.zeros((int(qs2[-1]), w.query_heads, w.head_dim), np.float16), qs2)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("accepted query_start[0] != 0")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

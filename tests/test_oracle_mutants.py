@@ -24,11 +24,11 @@ MUTANTS = {
     "layout_kv_before_slot": (
         "return ((page * p->page_size + slot) * (int64_t)p->kv_heads + kv) * p->head_dim;",
         "return ((page * p->kv_heads + kv) * (int64_t)p->page_size + slot) * p->head_dim;"),
-    "query_transposed": ("q + ((int64_t)b * p->query_heads + h) * p->head_dim;",
-                         "q + ((int64_t)h * p->batch + b) * p->head_dim;"),
+    "query_transposed": ("return attend(p, q + row * p->head_dim,",
+                         "return attend(p, q + ((int64_t)h * p->batch + b) * p->head_dim,"),
     "no_normalisation": ("for (int d = 0; d < hd; ++d) out[d] /= l;", ""),
     "exp_sign": ("double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
-    "context_short": ("int n = ctx[b];", "int n = ctx[b] > 0 ? ctx[b] - 1 : 0;"),
+    "context_short": ("b, h, ctx[b], scale, out);", "b, h, ctx[b] > 0 ? ctx[b] - 1 : 0, scale, out);"),
     "merge_alpha_sign": ("double alpha = (M == -INFINITY) ? 0.0 : exp(M - Mn);",
                          "double alpha = (M == -INFINITY) ? 0.0 : exp(Mn - M);"),
     "merge_no_skip": ("if (l[i] == 0.0) continue;", ""),
@@ -42,6 +42,14 @@ MUTANTS = {
                         "int64_t dst = cache_row(&p, page, (t + 1) % page_size, kv);"),
     "append_src_transposed": ("int64_t src = ((int64_t)b * kv_heads + kv) * head_dim;",
                               "int64_t src = ((int64_t)kv * batch + b) * head_dim;"),
+    "prefill_excludes_self": ("rc = attend(&p, query + r * head_dim, key_cache, value_cache, block_tables, b, h, pos + 1,",
+                              "rc = attend(&p, query + r * head_dim, key_cache, value_cache, block_tables, b, h, pos,"),
+    "prefill_no_prefix": ("int pos = context_lengths[b] - nb + (qi - query_start[b]);",
+                          "int pos = qi - query_start[b];"),
+    "prefill_sequence_lookup": ("while (query_start[b + 1] <= qi) ++b;",
+                                "while (query_start[b + 1] < qi) ++b;"),
+    "prefill_query_head0": ("rc = attend(&p, query + r * head_dim,",
+                            "rc = attend(&p, query + (int64_t)qi * query_heads * head_dim,"),
     "value_from_key": ("const uint16_t *vrow = value + cache_row", "const uint16_t *vrow = key + cache_row"),
 }
 
