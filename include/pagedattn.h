@@ -85,6 +85,8 @@ typedef enum pa_status_t {
 #define PA_DEVERR_PAGE_ID 1u /* a needed block-table entry was outside the page pool */
 #define PA_DEVERR_CONTEXT 2u /* a context length was < 0 or > max_pages*page_size */
 #define PA_DEVERR_TIMEOUT 4u /* a pipeline wait ran past its time limit; output invalid */
+#define PA_DEVERR_QUERY_START 8u /* pa_prefill: query offsets decreasing, past total_tokens,
+                                   or more new tokens than context */
 
 /* How work is split across the GPU. */
 typedef enum pa_schedule_t {
@@ -256,6 +258,34 @@ pa_status_t pa_split_kv_combine(const pa_problem_t *problem, int32_t num_splits,
 pa_status_t pa_append_kv(const pa_problem_t *problem, const void *new_key, const void *new_value,
                          const int32_t *block_tables, const int32_t *context_lengths,
                          void *key_cache, void *value_cache, void *stream);
+
+/* Causal multi-token (prefill) attention over the paged caches: the decode step of
+ * section "Paged Attention" extended to several new tokens per sequence, computed
+ * flash-style ("[TIL] Optimizing paged attention", section "Flash Attention": score
+ * tiles, an online softmax and the weighted value sum, never materialising the score
+ * matrix). Sequence b has n_b = query_start[b + 1] - query_start[b] new tokens whose K and V
+ * are already in the cache (written before the call, e.g. by pa_append_kv or a bulk copy):
+ * they are the last n_b of its context_lengths[b] tokens, so the j-th new token sits at
+ * position p = context_lengths[b] - n_b + j and attends to tokens 0..p.
+ *   query        fp16 [total_tokens][query_heads][head_dim], device, 16-byte aligned; row
+ *                query_start[b] + j is the j-th new token of sequence b
+ *   query_start  int32 [batch + 1], device, non-decreasing, query_start[0] = 0 and
+ *                query_start[batch] <= total_tokens
+ *   max_query_len  host int >= every n_b (sizes the grid; tokens past it are not computed)
+ *   key_cache, value_cache, block_tables, context_lengths, scale  as for pa_decode
+ *   out          fp32 [total_tokens][query_heads][head_dim], device, 16-byte aligned; rows of
+ *                new tokens are written, other rows are left untouched
+ *   options      may be NULL; only test_flags is read (other fields must be zero)
+ * Supports head_dim 64, 128 and 256 and query_heads / kv_heads <= 128. A sequence with
+ * inconsistent offsets is skipped and flagged (PA_DEVERR_QUERY_START), one with a context
+ * length out of range likewise (PA_DEVERR_CONTEXT); a needed page id outside the pool is
+ * flagged (PA_DEVERR_PAGE_ID) and its rows are invalid. Runs asynchronously on `stream`;
+ * allocates nothing. */
+pa_status_t pa_prefill(const pa_problem_t *problem, const void *query, const int32_t *query_start,
+                       int64_t total_tokens, int32_t max_query_len, const void *key_cache,
+                       const void *value_cache, const int32_t *block_tables,
+                       const int32_t *context_lengths, float scale, float *out,
+                       const pa_options_t *options, void *stream);
 
 /* Read and clear the device error word of the current device (PA_DEVERR_* bits) after
  * the work queued on `stream` finishes. Synchronises `stream`. */

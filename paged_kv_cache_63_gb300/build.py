@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpagedattn.so")
-SOURCES = ["api.cpp", "launch.cu", "noalloc.cu", "append.cu", "decode_hd64.cu",
+SOURCES = ["api.cpp", "launch.cu", "noalloc.cu", "append.cu", "prefill.cu", "decode_hd64.cu",
            "decode_hd128.cu", "decode_hd256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

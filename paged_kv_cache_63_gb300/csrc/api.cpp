@@ -264,6 +264,46 @@ pa_status_t encode_cache_map(CUtensorMap *map, const void *base, const pa_proble
   return rc == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+}  // namespace
+
+namespace pa {
+
+pa_status_t encode_cache_map_rows(CUtensorMap *map, const void *base, const pa_problem_t *p,
+                                  int rows_per_box) {
+  return encode_cache_map(map, base, p, rows_per_box);
+}
+
+pa_status_t encode_query_map(CUtensorMap *map, const void *query, int64_t total_tokens,
+                             int query_heads, int head_dim, int heads_per_box, int tokens_per_box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  const cuuint64_t hd = static_cast<cuuint64_t>(head_dim);
+  cuuint64_t dims[3] = {hd, static_cast<cuuint64_t>(query_heads),
+                        static_cast<cuuint64_t>(total_tokens > 0 ? total_tokens : 1)};
+  cuuint64_t strides[2] = {hd * 2, static_cast<cuuint64_t>(query_heads) * hd * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(heads_per_box),
+                       static_cast<cuuint32_t>(tokens_per_box)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(query), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return rc == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status_t check_problem_public(const pa_problem_t *p) { return check_problem(p); }
+
+pa_status_t current_device_smem(int *smem_optin) {
+  int dev = 0;
+  DeviceInfo di;
+  pa_status_t st = current_device(&dev, &di);
+  if (st == PA_OK) *smem_optin = di.smem_optin;
+  return st;
+}
+
+}  // namespace pa
+
+namespace {
+
 // ---- merge counters -------------------------------------------------------------------
 // The fused merge keeps one counter per unit at the start of the workspace; a call leaves
 // the counters it used at zero, but its partial states overwrite whatever lies past them.

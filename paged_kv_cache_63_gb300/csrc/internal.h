@@ -125,6 +125,16 @@ pa_status_t validate_call(const pa_problem_t *p, const pa_options_t *o, const vo
                           const void *k, const void *v, const int32_t *bt, const int32_t *ctx,
                           float scale, const float *out);
 
+// Tensor maps (api.cpp): a cache map whose box is rows_per_box rows of one head; a query map
+// over [total_tokens][query_heads][head_dim] whose box is 64 x heads_per_box x tokens_per_box.
+pa_status_t encode_cache_map_rows(CUtensorMap *map, const void *base, const pa_problem_t *p,
+                                  int rows_per_box);
+pa_status_t encode_query_map(CUtensorMap *map, const void *query, int64_t total_tokens,
+                             int query_heads, int head_dim, int heads_per_box, int tokens_per_box);
+pa_status_t check_problem_public(const pa_problem_t *p);
+// The current device's opt-in shared memory per block; PA_ERR_NO_DEVICE unless sm_103.
+pa_status_t current_device_smem(int *smem_optin);
+
 // One decode step: validation, plan, workspace checks, tensor maps and launches.
 pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, const void *v,
                         const int32_t *bt, const int32_t *ctx, float scale, float *out,

@@ -1,0 +1,453 @@
+// prefill_kernel.cuh -- causal multi-token attention over the paged K/V cache on the
+// tcgen05 tensor cores ("[TIL] Optimizing paged attention", section "Flash Attention":
+// scores of a block of query rows against a tile of keys, an online softmax, and the
+// weighted sum of the tile's values, applied to the paged cache of section "Paged
+// Attention" with a causal limit per query row).
+//
+// One CTA owns one (sequence b, K/V head, query tile): 128 MMA rows holding QT new tokens x
+// g query heads (row = token * g + head, QT = 128 / g), so the K/V tile in shared memory
+// serves every query head that reads it. Per K/V tile of TN tokens:
+//   S = Q K^T        128 x TN   fp32 in TMEM (two buffers, so S(j+1) overlaps softmax(j))
+//   P = exp2(S*scale*log2e - m)  fp16 in shared memory (two buffers)
+//   O += P V         128 x HD   fp32 in TMEM
+// Warp roles (6 warps): 0 loads Q, K and V with TMA; 1 owns TMEM and issues the MMAs from
+// one thread; 2..5 run the softmax, one query row per thread (TMEM lane = row), rescale O in
+// TMEM when a row's running maximum grows by more than 2^8, and write the output.
+// Every mbarrier wait is bounded; a wait that expires raises PA_DEVERR_TIMEOUT, the other
+// roles stop at their next wait, in-flight copies and MMAs are drained and TMEM is freed.
+#pragma once
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace pa {
+
+struct PrefillArgs {
+  const int32_t *qs;   // [batch + 1] first query row of each sequence
+  const int32_t *bt;   // [batch][maxp]
+  const int32_t *ctx;  // [batch] tokens in the cache, the new ones included
+  float *out;          // [total][qh][hd]
+  unsigned *err;
+  long long total;  // rows of query and out
+  int batch, qh, kvh, ps, ps_shift, maxp, num_pages, layout;
+  int g;         // query heads per K/V head
+  int qt;        // new tokens per query tile (128 / g)
+  int n_qtiles;  // grid.z
+  float scale_log2;
+  int expire;  // PA_TEST_EXPIRE_WAITS: the MMA warp's first wait is on a barrier that
+               // completes only at the end, so it runs out
+};
+
+template <int HD>
+struct PrefillCfg {
+  static constexpr int kRows = 128;                // MMA M
+  static constexpr int KB = HD / 64;               // 64-element (128-byte) column blocks
+  static constexpr int TN = HD == 256 ? 64 : 128;  // K/V tokens per tile
+  static constexpr int kStages = 2;
+  static constexpr int kQBytes = KB * kRows * 128;
+  static constexpr int kKVBytes = TN * HD * 2;     // one K (or V) stage
+  static constexpr int kPBytes = kRows * TN * 2;   // one P buffer
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kQBytes;
+  static constexpr int kVOff = kKOff + kStages * kKVBytes;
+  static constexpr int kPOff = kVOff + kStages * kKVBytes;
+  static constexpr int kSmem = kPOff + 2 * kPBytes;  // the launch adds 1 KB for alignment
+  static constexpr int kOCol = 256;                  // O columns [256, 256 + HD); S at 0 and TN
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kIdescS = idesc_f16(kRows, TN, 0, 0);
+  static constexpr uint32_t kIdescPV = idesc_f16(kRows, HD, 0, 1);
+};
+
+constexpr int kPrefillThreads = 192;
+constexpr float kPrefillRescaleSlack = 8.f;  // log2 units: O is rescaled when m grows > 2^8
+
+// Barrier slots.
+enum : int {
+  kBarQ = 0,
+  kBarKFull = 1,   // +stage
+  kBarKEmpty = 3,  // +stage
+  kBarVFull = 5,
+  kBarVEmpty = 7,
+  kBarSFull = 9,   // +buffer
+  kBarPFull = 11,  // +buffer (128 arrivals: the softmax threads)
+  kBarPV = 13,     // +buffer: the P.V MMAs of that buffer completed
+  kBarDone = 15,
+  kNumBars = 16
+};
+
+__device__ __forceinline__ float prefill_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Warp-collective bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool pipe_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned *err) {
+  bool ok = mbar_try_wait(bar, parity);
+  bool expired = false;
+  if (!ok) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if ((i & 31u) == 0) {
+        if (*abort_flag) break;
+        if (global_ns() - t0 > kWaitLimitNs) {
+          expired = true;
+          break;
+        }
+      }
+    }
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  expired = __any_sync(0xffffffffu, expired);
+  if (!ok && (threadIdx.x & 31) == 0) {
+    if (expired) atomicOr(err, PA_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  return ok;
+}
+
+// Bounded wait used while draining (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+  bool ok = mbar_try_wait(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+      if (mbar_try_wait(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if ((i & 31u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  if (!ok) atomicOr(err, PA_DEVERR_TIMEOUT);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using C = PrefillCfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_word;
+  volatile int *abort_flag = &abort_word;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv = blockIdx.x, b = blockIdx.y;
+  const int qtile = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);  // longest rows first
+
+  // ---- sequence geometry (uniform over the CTA) ----
+  const int q0 = __ldg(a.qs + b), q1 = __ldg(a.qs + b + 1), ctx = __ldg(a.ctx + b);
+  const int n = q1 - q0;
+  if (ctx < 0 || static_cast<long long>(ctx) > static_cast<long long>(a.maxp) << a.ps_shift) {
+    if (threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_CONTEXT);
+    return;
+  }
+  if (q0 < 0 || n < 0 || static_cast<long long>(q1) > a.total || n > ctx) {
+    if (threadIdx.x == 0) atomicOr(a.err, PA_DEVERR_QUERY_START);
+    return;
+  }
+  const int tok0 = qtile * a.qt;
+  if (tok0 >= n) return;
+  const int base_pos = ctx - n + tok0;                        // position of the tile's token 0
+  const int max_pos = ctx - n + min(tok0 + a.qt, n) - 1;      // last position any row sees
+  const int kv_len = max_pos + 1;
+  const int ntiles = (kv_len + C::TN - 1) / C::TN;
+  const int q_rows = a.qt * a.g;
+
+  const uint32_t sbase = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  uint8_t *sgen = smem_raw + (sbase - smem_addr(smem_raw));
+  const uint32_t sq = sbase + C::kQOff;
+  auto k_stage = [&](int s) { return sbase + C::kKOff + s * C::kKVBytes; };
+  auto v_stage = [&](int s) { return sbase + C::kVOff + s * C::kKVBytes; };
+  auto p_buf = [&](int s) { return sbase + C::kPOff + s * C::kPBytes; };
+  auto bar = [&](int i) { return smem_addr(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 128 : 1);
+    abort_word = 0;
+    fence_barrier_init();
+  }
+  // Rows of Q past q_rows are never loaded: zero them so their (discarded) results stay finite.
+  if (q_rows < C::kRows) {
+    const int per_block = (C::kRows - q_rows) * 8;  // 16-byte chunks
+    for (int i = threadIdx.x; i < C::KB * per_block; i += kPrefillThreads) {
+      const int kb = i / per_block, c = i % per_block;
+      *reinterpret_cast<uint4 *>(sgen + C::kQOff + kb * (C::kRows * 128) + q_rows * 128 + c * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ================= producer: TMA loads of Q, then K and V tiles =================
+    if (lane == 0) {
+      prefetch_tensormap(&tq);
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+      mbar_arrive_expect_tx(bar(kBarQ), C::KB * q_rows * 128);
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_3d_plain(sq + kb * (C::kRows * 128), &tq, bar(kBarQ), kb * 64, kv * a.g,
+                          q0 + tok0);
+    }
+    const int rows_per_box = min(a.ps, C::TN);
+    const int boxes = C::TN / rows_per_box;
+    const uint32_t box_bytes = rows_per_box * 128;
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int st = j & 1;
+      // page of this lane's box (lanes < boxes); boxes past the last needed token are skipped
+      const int tok = j * C::TN + lane * rows_per_box;
+      int page = -1;
+      if (lane < boxes && tok < kv_len) {
+        page = __ldg(a.bt + static_cast<size_t>(b) * a.maxp + (tok >> a.ps_shift));
+        if (page < 0 || page >= a.num_pages) {
+          atomicOr(a.err, PA_DEVERR_PAGE_ID);
+          page = -1;
+        }
+      }
+      const uint32_t issue = __ballot_sync(0xffffffffu, page >= 0);
+      const int slot = tok & (a.ps - 1);
+      int y, z;
+      if (a.layout == PA_LAYOUT_HEAD_MAJOR) {
+        y = slot;
+        z = page * a.kvh + kv;
+      } else {
+        y = kv;
+        z = (page << a.ps_shift) + slot;
+      }
+      const uint32_t tx = __popc(issue) * box_bytes * C::KB;
+      // K
+      if (j >= 2) ok = pipe_wait(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), tx);
+      __syncwarp();
+      if (page >= 0) {
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d_plain(k_stage(st) + kb * (C::TN * 128) + lane * box_bytes, &tk,
+                            bar(kBarKFull + st), kb * 64, y, z);
+      }
+      k_issued = j + 1;
+      // V
+      if (j >= 2) ok = pipe_wait(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), tx);
+      __syncwarp();
+      if (page >= 0) {
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d_plain(v_stage(st) + kb * (C::TN * 128) + lane * box_bytes, &tv,
+                            bar(kBarVFull + st), kb * 64, y, z);
+      }
+      v_issued = j + 1;
+    }
+    // drain: the last load issued into each stage, and Q, have landed before the CTA exits
+    if (lane == 0) {
+      drain_wait(bar(kBarQ), 0, a.err);
+      for (int j = max(0, k_issued - 2); j < k_issued; ++j) drain_wait(bar(kBarKFull + (j & 1)), (j >> 1) & 1, a.err);
+      for (int j = max(0, v_issued - 2); j < v_issued; ++j) drain_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1, a.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    // (under PA_TEST_EXPIRE_WAITS: wait on kBarDone, which no one completes before the end)
+    bool ok = pipe_wait(bar(a.expire ? kBarDone : kBarQ), 0, abort_flag, a.err);
+    const int rows_last = kv_len - (ntiles - 1) * C::TN;  // valid rows of the last V tile
+    for (int j = 0; j <= ntiles && ok; ++j) {
+      if (j < ntiles) {
+        const int st = j & 1;
+        ok = pipe_wait(bar(kBarKFull + st), (j >> 1) & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + st * C::TN;
+#pragma unroll
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * (C::TN * 128) + (ks & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(sq + (ks >> 2) * (C::kRows * 128) + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(k_stage(st) + off, 16, 1024);
+            mma_f16_ss(d, ad, bd, C::kIdescS, ks > 0);
+          }
+          mma_commit(bar(kBarSFull + st));
+          mma_commit(bar(kBarKEmpty + st));
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int i = j - 1, st = i & 1;
+        ok = pipe_wait(bar(kBarPFull + st), (i >> 1) & 1, abort_flag, a.err);
+        if (ok) ok = pipe_wait(bar(kBarVFull + st), (i >> 1) & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc_fence_after();
+        if (i == ntiles - 1 && rows_last < C::TN) {
+          // V rows past the last needed token hold unread cache slots (possibly never
+          // written); P is zero there, but 0 * NaN is not, so clear them.
+          const int per_block = (C::TN - rows_last) * 8;
+          uint8_t *vg = sgen + C::kVOff + st * C::kKVBytes;
+          for (int c = lane; c < C::KB * per_block; c += 32) {
+            const int kb = c / per_block, r = c % per_block;
+            *reinterpret_cast<uint4 *>(vg + kb * (C::TN * 128) + rows_last * 128 + r * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < C::TN / 16; ++ks) {
+            const uint64_t ad = smem_desc_sw128(p_buf(st) + (ks >> 2) * (C::kRows * 128) + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(v_stage(st) + ks * 2048, C::TN * 128, 1024);
+            mma_f16_ss(tmem + C::kOCol, ad, bd, C::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarPV + st));
+          mma_commit(bar(kBarVEmpty + st));
+        }
+        __syncwarp();
+      }
+    }
+    // every MMA this thread issued has completed before TMEM is released
+    if (lane == 0) {
+      mma_commit(bar(kBarDone));
+      drain_wait(bar(kBarDone), 0, a.err);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax: one query row per thread =================
+    const int rg = warp & 3;
+    const int row = rg * 32 + lane;
+    const int t = row / a.g, h = row - t * a.g;
+    const bool valid = row < q_rows && tok0 + t < n;
+    const int pos = min(base_pos + t, max_pos);
+    const uint32_t trow = tmem + (static_cast<uint32_t>(rg * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      ok = pipe_wait(bar(kBarSFull + st), (j >> 1) & 1, abort_flag, a.err);
+      if (!ok) break;
+      tc_fence_after();
+      float x[C::TN];
+#pragma unroll
+      for (int c = 0; c < C::TN / 32; ++c) {
+        float v[32];
+        tmem_ld32(trow + st * C::TN + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+      }
+      // scaled scores (log2 units); keys past this row's position are masked out
+      const int lim = pos - j * C::TN;
+      float mx = -INFINITY;
+      if (lim >= C::TN - 1) {
+#pragma unroll
+        for (int c = 0; c < C::TN; ++c) {
+          x[c] *= sl2;
+          mx = fmaxf(mx, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::TN; ++c) {
+          x[c] = c <= lim ? x[c] * sl2 : -INFINITY;
+          mx = fmaxf(mx, x[c]);
+        }
+      }
+      const bool grow = mx > m + kPrefillRescaleSlack;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float mnew = grow ? mx : m;
+        // 0 on the first tile (m = -inf); 1 for rows whose maximum did not grow
+        const float f = mnew == -INFINITY ? 1.f : prefill_exp2(m - mnew);
+        l *= f;
+        if (j > 0) {
+          // O holds tiles < j: wait for the last P.V, then scale this row of O in TMEM
+          ok = pipe_wait(bar(kBarPV + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            float v[32];
+            tmem_ld32(trow + C::kOCol + c * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] *= f;
+            tmem_st32(trow + C::kOCol + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        m = mnew;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < C::TN; ++c) {
+        x[c] = prefill_exp2(x[c] - m);
+        rs += x[c];
+      }
+      l += rs;
+      // P buffer st was last read by the P.V of tile j - 2
+      if (j >= 2) {
+        ok = pipe_wait(bar(kBarPV + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
+        if (!ok) break;
+      }
+      const uint32_t prow = p_buf(st) + row * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < C::TN / 8; ++c8) {
+        uint4 w;
+        w.x = pack_half2(x[c8 * 8 + 0], x[c8 * 8 + 1]);
+        w.y = pack_half2(x[c8 * 8 + 2], x[c8 * 8 + 3]);
+        w.z = pack_half2(x[c8 * 8 + 4], x[c8 * 8 + 5]);
+        w.w = pack_half2(x[c8 * 8 + 6], x[c8 * 8 + 7]);
+        sts128(prow + (c8 >> 3) * (C::kRows * 128) + (((c8 & 7) ^ (row & 7)) << 4), w);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPFull + st));
+    }
+    if (ok) {
+      const int i = ntiles - 1;
+      ok = pipe_wait(bar(kBarPV + (i & 1)), (i >> 1) & 1, abort_flag, a.err);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float *dst = a.out + (static_cast<size_t>(q0 + tok0 + t) * a.qh + kv * a.g + h) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        float v[32];
+        tmem_ld32(trow + C::kOCol + c * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(dst + c * 32 + e) =
+                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace pa

@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 PA_DEVERR_PAGE_ID = 1
 PA_DEVERR_CONTEXT = 2
 PA_DEVERR_TIMEOUT = 4
+PA_DEVERR_QUERY_START = 8
 PA_TEST_EXPIRE_WAITS = 1
 SCHEDULE = {"auto": 0, "single": 1, "balanced": 2}
 MATH = {"auto": 0, "simt": 1, "mma": 2}
@@ -30,7 +31,7 @@ COMBINE = {"auto": 0, "fused": 1, "kernel": 2}
 
 # Every entry point include/pagedattn.h declares.
 EXPORTS = ("pa_plan", "pa_workspace_size", "pa_workspace_init", "pa_decode", "pa_decode_ex",
-           "pa_decode_noalloc", "pa_append_kv",
+           "pa_decode_noalloc", "pa_append_kv", "pa_prefill",
            "pa_split_kv_partial", "pa_split_kv_combine", "pa_get_device_error",
            "pa_status_string", "pa_version")
 
@@ -91,6 +92,8 @@ def load(path: Optional[str] = None):
                                      vp, ctypes.c_size_t, vp]
         lib.pa_decode_noalloc.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, vp, vp]
         lib.pa_append_kv.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, vp, vp]
+        lib.pa_prefill.argtypes = [P(pa_problem_t), vp, vp, ctypes.c_int64, i32, vp, vp, vp, vp,
+                                   f32, vp, P(pa_options_t), vp]
         lib.pa_split_kv_partial.argtypes = [P(pa_problem_t), vp, vp, vp, vp, vp, f32, i32, i32, vp,
                                             vp, vp, vp]
         lib.pa_split_kv_combine.argtypes = [P(pa_problem_t), i32, vp, vp, vp, vp, vp]
@@ -215,6 +218,19 @@ def pa_append_kv(prob, new_key, new_value, block_tables, context_lengths, key_ca
     _check(load().pa_append_kv(ctypes.byref(prob), _ptr(new_key), _ptr(new_value),
                                _ptr(block_tables), _ptr(context_lengths), _ptr(key_cache),
                                _ptr(value_cache), _stream(stream)), "pa_append_kv")
+
+
+def pa_prefill(prob, query, query_start, total_tokens, max_query_len, key_cache, value_cache,
+               block_tables, context_lengths, scale, out, opts: Optional[pa_options_t] = None,
+               stream=None):
+    """Causal attention of each sequence's last n_b tokens (query rows query_start[b] ..
+    query_start[b + 1]) over its paged cache; fp32 out [total_tokens][query_heads][head_dim]."""
+    _check(load().pa_prefill(ctypes.byref(prob), _ptr(query), _ptr(query_start),
+                             int(total_tokens), int(max_query_len), _ptr(key_cache),
+                             _ptr(value_cache), _ptr(block_tables), _ptr(context_lengths),
+                             float(scale), _ptr(out),
+                             ctypes.byref(opts) if opts is not None else None,
+                             _stream(stream)), "pa_prefill")
 
 
 def pa_split_kv_partial(prob, query, key_cache, value_cache, block_tables, context_lengths, scale,
