@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and μs per call"
 DEFAULT_WORKLOAD = "gqa4_mid"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["device_common.cuh", "decode_kernel.cuh", "decode_launch.cuh", "internal.h",
                   "api.cpp", "launch.cu"]
@@ -234,6 +235,69 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
     return ms, wall, clocks
 
 
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor peak (TFLOP/s): the measured bf16 GEMM burst figure (fp16 and
+    bf16 share one dense rate on these tensor cores)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def time_prefill(p, steps, warmup, torch, lib):
+    """Mean CUDA-event time (ms) of one pa_prefill call, L2 flushed before each call."""
+    w = p.cache
+    d = [torch.from_numpy(x).cuda() for x in (p.query, p.query_start, w.key_cache, w.value_cache,
+                                               w.block_tables, w.context_lengths)]
+    out = torch.empty((p.total, w.query_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    prob = lib.problem_of(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lib.pa_prefill(prob, d[0], d[1], p.total, p.max_query_len(), d[2], d[3], d[4], d[5],
+                       w.scale, out, None, stream.cuda_stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    return sum(ms) / len(ms)
+
+
+def prefill_lines(torch, lib, steps):
+    """The multi-token (prefill) kernel on its workloads, against the dense tensor peak."""
+    from paged_kv_cache_63_gb300.workloads import make_prefill
+
+    peak, kind = measured_tensor_peak()
+    res = {}
+    for name in ("prefill_gqa4", "prefill_chunked", "prefill_mha"):
+        p = make_prefill(name)
+        ms = time_prefill(p, steps, 5, torch, lib)
+        assert lib.pa_get_device_error() == 0
+        flops = 4.0 * p.causal_pairs() * p.cache.query_heads * p.cache.head_dim
+        tf = flops / (ms * 1e-3) / 1e12
+        res[name] = {"us_per_call": round(ms * 1e3, 1), "tflops": round(tf, 1),
+                     "causal_flops": flops,
+                     "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                                  "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                                  "peak_source": f"{kind} (bf16 GEMM burst; fp16 same rate)",
+                                  "kernel": "pa::prefill_kernel"}}
+        torch.cuda.empty_cache()
+    return res
+
+
 def reduce_over_ranks(torch, device, maxima, sums):
     """Whole-job figures for weak scaling: the slowest rank's times (max over ranks) and the
     bytes all ranks moved (sum). With one process the values pass through."""
@@ -381,6 +445,7 @@ def run_ours(args):
             del do
             torch.cuda.empty_cache()
         line["other_workloads"] = others
+        line["prefill"] = prefill_lines(torch, lib, 20)
     line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:

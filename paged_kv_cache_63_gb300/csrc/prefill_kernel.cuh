@@ -10,8 +10,8 @@
 //   S = Q K^T        128 x TN   fp32 in TMEM (two buffers, so S(j+1) overlaps softmax(j))
 //   P = exp2(S*scale*log2e - m)  fp16 in shared memory (two buffers)
 //   O += P V         128 x HD   fp32 in TMEM
-// Warp roles (6 warps): 0 loads Q, K and V with TMA; 1 owns TMEM and issues the MMAs from
-// one thread; 2..5 run the softmax, one query row per thread (TMEM lane = row), rescale O in
+// Warp roles (7 warps): 0 loads Q and K with TMA, 6 loads V; 1 owns TMEM and issues the
+// MMAs from one thread; 2..5 run the softmax, one query row per thread (TMEM lane = row), rescale O in
 // TMEM when a row's running maximum grows by more than 2^8, and write the output.
 // Every mbarrier wait is bounded; a wait that expires raises PA_DEVERR_TIMEOUT, the other
 // roles stop at their next wait, in-flight copies and MMAs are drained and TMEM is freed.
@@ -59,7 +59,8 @@ struct PrefillCfg {
   static constexpr uint32_t kIdescPV = idesc_f16(kRows, HD, 0, 1);
 };
 
-constexpr int kPrefillThreads = 192;
+constexpr int kPrefillThreads = 224;
+constexpr int kPrefillVWarp = 6;
 constexpr float kPrefillRescaleSlack = 8.f;  // log2 units: O is rescaled when m grows > 2^8
 
 // Barrier slots.
@@ -198,34 +199,45 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 0) {
-    // ================= producer: TMA loads of Q, then K and V tiles =================
+  if (warp == 0 || warp == kPrefillVWarp) {
+    // ============ producers: warp 0 loads Q and the K tiles, the last warp the V tiles ============
+    const bool is_v = warp == kPrefillVWarp;
     if (lane == 0) {
-      prefetch_tensormap(&tq);
-      prefetch_tensormap(&tk);
-      prefetch_tensormap(&tv);
-      mbar_arrive_expect_tx(bar(kBarQ), C::KB * q_rows * 128);
+      prefetch_tensormap(is_v ? &tv : &tk);
+      if (!is_v) {
+        prefetch_tensormap(&tq);
+        mbar_arrive_expect_tx(bar(kBarQ), C::KB * q_rows * 128);
 #pragma unroll
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d_plain(sq + kb * (C::kRows * 128), &tq, bar(kBarQ), kb * 64, kv * a.g,
-                          q0 + tok0);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d_plain(sq + kb * (C::kRows * 128), &tq, bar(kBarQ), kb * 64, kv * a.g,
+                            q0 + tok0);
+      }
     }
+    const CUtensorMap *map = is_v ? &tv : &tk;
+    const int full = is_v ? kBarVFull : kBarKFull;
+    const int empty = is_v ? kBarVEmpty : kBarKEmpty;
+    const uint32_t stage0 = is_v ? v_stage(0) : k_stage(0);
     const int rows_per_box = min(a.ps, C::TN);
     const int boxes = C::TN / rows_per_box;
     const uint32_t box_bytes = rows_per_box * 128;
-    int k_issued = 0, v_issued = 0;
+    const int32_t *bt_row = a.bt + static_cast<size_t>(b) * a.maxp;
+    // page of this lane's box of tile j (lanes < boxes); -1 past the last needed token
+    auto page_of = [&](int j) {
+      const int tok = j * C::TN + lane * rows_per_box;
+      return (j < ntiles && lane < boxes && tok < kv_len) ? __ldg(bt_row + (tok >> a.ps_shift)) : -1;
+    };
+    int issued = 0;
     bool ok = true;
+    // the block-table read for tile j + 1 is issued before the waits of tile j, hiding its latency
+    int page_next = page_of(0);
     for (int j = 0; j < ntiles && ok; ++j) {
       const int st = j & 1;
-      // page of this lane's box (lanes < boxes); boxes past the last needed token are skipped
       const int tok = j * C::TN + lane * rows_per_box;
-      int page = -1;
-      if (lane < boxes && tok < kv_len) {
-        page = __ldg(a.bt + static_cast<size_t>(b) * a.maxp + (tok >> a.ps_shift));
-        if (page < 0 || page >= a.num_pages) {
-          atomicOr(a.err, PA_DEVERR_PAGE_ID);
-          page = -1;
-        }
+      int page = page_next;
+      page_next = page_of(j + 1);
+      if (lane < boxes && tok < kv_len && (page < 0 || page >= a.num_pages)) {
+        if (!is_v) atomicOr(a.err, PA_DEVERR_PAGE_ID);
+        page = -1;
       }
       const uint32_t issue = __ballot_sync(0xffffffffu, page >= 0);
       const int slot = tok & (a.ps - 1);
@@ -237,37 +249,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         y = kv;
         z = (page << a.ps_shift) + slot;
       }
-      const uint32_t tx = __popc(issue) * box_bytes * C::KB;
-      // K
-      if (j >= 2) ok = pipe_wait(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
+      if (j >= 2) ok = pipe_wait(bar(empty + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + st), tx);
+      if (lane == 0) mbar_arrive_expect_tx(bar(full + st), __popc(issue) * box_bytes * C::KB);
       __syncwarp();
       if (page >= 0) {
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d_plain(k_stage(st) + kb * (C::TN * 128) + lane * box_bytes, &tk,
-                            bar(kBarKFull + st), kb * 64, y, z);
+          tma_load_3d_plain(stage0 + st * C::kKVBytes + kb * (C::TN * 128) + lane * box_bytes, map,
+                            bar(full + st), kb * 64, y, z);
       }
-      k_issued = j + 1;
-      // V
-      if (j >= 2) ok = pipe_wait(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + st), tx);
-      __syncwarp();
-      if (page >= 0) {
-#pragma unroll
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d_plain(v_stage(st) + kb * (C::TN * 128) + lane * box_bytes, &tv,
-                            bar(kBarVFull + st), kb * 64, y, z);
-      }
-      v_issued = j + 1;
+      issued = j + 1;
     }
     // drain: the last load issued into each stage, and Q, have landed before the CTA exits
     if (lane == 0) {
-      drain_wait(bar(kBarQ), 0, a.err);
-      for (int j = max(0, k_issued - 2); j < k_issued; ++j) drain_wait(bar(kBarKFull + (j & 1)), (j >> 1) & 1, a.err);
-      for (int j = max(0, v_issued - 2); j < v_issued; ++j) drain_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1, a.err);
+      if (!is_v) drain_wait(bar(kBarQ), 0, a.err);
+      for (int j = max(0, issued - 2); j < issued; ++j) drain_wait(bar(full + (j & 1)), (j >> 1) & 1, a.err);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -359,20 +356,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       // scaled scores (log2 units); keys past this row's position are masked out
       const int lim = pos - j * C::TN;
-      float mx = -INFINITY;
+      // eight independent partial maxima and sums keep the reductions off one dependency chain
+      float mp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
       if (lim >= C::TN - 1) {
 #pragma unroll
         for (int c = 0; c < C::TN; ++c) {
           x[c] *= sl2;
-          mx = fmaxf(mx, x[c]);
+          mp[c & 7] = fmaxf(mp[c & 7], x[c]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < C::TN; ++c) {
           x[c] = c <= lim ? x[c] * sl2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
+          mp[c & 7] = fmaxf(mp[c & 7], x[c]);
         }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const bool grow = mx > m + kPrefillRescaleSlack;
       if (__any_sync(0xffffffffu, grow)) {
         const float mnew = grow ? mx : m;
@@ -396,13 +398,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         m = mnew;
       }
-      float rs = 0.f;
+      float rp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rp[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < C::TN; ++c) {
         x[c] = prefill_exp2(x[c] - m);
-        rs += x[c];
+        rp[c & 7] += x[c];
       }
-      l += rs;
+      l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       // P buffer st was last read by the P.V of tile j - 2
       if (j >= 2) {
         ok = pipe_wait(bar(kBarPV + st), ((j >> 1) - 1) & 1, abort_flag, a.err);
