@@ -4,6 +4,7 @@
 
 #include "internal.h"
 #include "pagedattn.h"
+#include "prefill2_kernel.cuh"
 #include "prefill_kernel.cuh"
 
 namespace pa {
@@ -28,6 +29,26 @@ cudaError_t launch_prefill_hd(const PrefillArgs &a, const CUtensorMap &tq, const
     if (dev >= 0 && dev < kMaxDevicesPrefill) set[dev] = true;
   }
   kern<<<grid, kPrefillThreads, smem, stream>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
+// head_dim 64 / 128: two query tiles per CTA (a.n_qtiles counts pairs, grid.z too)
+template <int HD>
+cudaError_t launch_prefill2_hd(const PrefillArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                               const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
+  using C = Prefill2Cfg<HD>;
+  auto kern = prefill2_kernel<HD>;
+  constexpr int smem = C::kSmem + 1024;
+  static bool set[kMaxDevicesPrefill] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevicesPrefill || !set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevicesPrefill) set[dev] = true;
+  }
+  kern<<<grid, kPrefill2Threads, smem, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 
@@ -106,15 +127,16 @@ extern "C" pa_status_t pa_prefill(const pa_problem_t *problem, const void *query
   st = encode_cache_map_rows(&tv, value_cache, problem, rows);
   if (st != PA_OK) return st;
 
-  const dim3 grid(a.kvh, a.batch, a.n_qtiles);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (hd != 256) a.n_qtiles = (a.n_qtiles + 1) / 2;  // pairs of query tiles
+  const dim3 grid(a.kvh, a.batch, a.n_qtiles);
   switch (hd) {
     case 64:
-      e = launch_prefill_hd<64>(a, tq, tk, tv, grid, s);
+      e = launch_prefill2_hd<64>(a, tq, tk, tv, grid, s);
       break;
     case 128:
-      e = launch_prefill_hd<128>(a, tq, tk, tv, grid, s);
+      e = launch_prefill2_hd<128>(a, tq, tk, tv, grid, s);
       break;
     case 256:
       e = launch_prefill_hd<256>(a, tq, tk, tv, grid, s);
