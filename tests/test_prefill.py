@@ -150,8 +150,9 @@ def test_prefill_full_size_sampled(name):
     assert_close(got[toks, heads], ref, name)
 
 
-def test_prefill_bad_offsets_flagged():
-    p = CASES["tiny"]()
+@pytest.mark.parametrize("name", ["tiny", "hd256_g6"])  # the two-tile and the single-tile kernel
+def test_prefill_bad_offsets_flagged(name):
+    p = CASES[name]()
     qs = p.query_start.copy()
     qs[1] = qs[2] + 1  # decreasing offsets
     _, flags = gpu_prefill(p, query_start=qs, check_errors=False)
@@ -161,19 +162,21 @@ def test_prefill_bad_offsets_flagged():
     assert_close(got, oracle.prefill(p.cache, p.query, p.query_start), "after bad offsets")
 
 
-def test_prefill_bad_page_flagged():
-    p = CASES["tiny"]()
+@pytest.mark.parametrize("name", ["tiny", "hd256_g6"])
+def test_prefill_bad_page_flagged(name):
+    p = CASES[name]()
     bt = p.cache.block_tables.copy()
-    bt[1, 2] = p.cache.num_physical_pages + 3
+    bt[0, 1] = p.cache.num_physical_pages + 3  # a page every sequence-0 query reads
     bad = dataclasses.replace(p, cache=dataclasses.replace(p.cache, block_tables=bt))
     _, flags = gpu_prefill(bad, check_errors=False)
     assert flags & lib.PA_DEVERR_PAGE_ID
 
 
-def test_prefill_expired_wait_reports_timeout():
+@pytest.mark.parametrize("name", ["tiny", "hd256_g6"])
+def test_prefill_expired_wait_reports_timeout(name):
     """A wait that runs out raises PA_DEVERR_TIMEOUT; the kernel drains and frees its tensor
     memory, so the next call on the same device is correct."""
-    p = CASES["tiny"]()
+    p = CASES[name]()
     opts = lib.options(test_flags=lib.PA_TEST_EXPIRE_WAITS)
     _, flags = gpu_prefill(p, opts=opts, check_errors=False)
     assert flags & lib.PA_DEVERR_TIMEOUT
