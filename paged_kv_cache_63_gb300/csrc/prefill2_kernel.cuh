@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
 #pragma unroll
       for (int x = 0; x < 2; ++x) {
         if (!ok || j >= nt_of(x)) continue;
+        // P_X(j) is released only after V(j) and K(j + 1) have landed (see the softmax)
         ok = pipe_wait(bar(kB2PFull + x), j & 1, abort_flag, a.err);
-        if (ok) ok = wait_item(2 * j + 1);
         if (!ok) break;
         tc_fence_after();
         if (x == 0 || j >= nt_a) clear_v_tail(j);
@@ -276,8 +276,6 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
         const bool last_v_user = (x == 1) || (j >= nt_b);
         if (last_v_user) release(2 * j + 1);
         if (j + 1 < nt_of(x)) {
-          ok = wait_item(2 * (j + 1));
-          if (!ok) break;
           issue_s(x, j + 1);
           const bool last_k_user = (x == 1) || (j + 1 >= nt_b);
           if (last_k_user) release(2 * (j + 1));
@@ -308,8 +306,27 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
       ok = pipe_wait(bar(kB2SFull + x), j & 1, abort_flag, a.err);
       if (!ok) break;
       tc_fence_after();
+      // The MMAs this P releases read V(j) and, for S(j + 1), K(j + 1): one warp of the
+      // group confirms they have landed before the group releases P, so the MMA warp waits
+      // on P alone. (Neither slot can be recycled first: both are released only after MMAs
+      // that need this P.) The probes go out before the score load and are read after it.
+      const int iv = 2 * j + 1, ik = 2 * j + 2;
+      bool kv_ready = true;
+      if (rg == 0) {
+        const bool rv = mbar_try_wait(bar(kB2Full + iv % C::kSlots), (iv / C::kSlots) & 1);
+        const bool rk = j + 1 < my_nt
+                            ? mbar_try_wait(bar(kB2Full + ik % C::kSlots), (ik / C::kSlots) & 1)
+                            : true;
+        kv_ready = rv && rk;
+      }
       float v[C::TN];
       tmem_ld128(ts, v);
+      if (rg == 0 && !__all_sync(0xffffffffu, kv_ready)) {
+        ok = pipe_wait(bar(kB2Full + iv % C::kSlots), (iv / C::kSlots) & 1, abort_flag, a.err);
+        if (ok && j + 1 < my_nt)
+          ok = pipe_wait(bar(kB2Full + ik % C::kSlots), (ik / C::kSlots) & 1, abort_flag, a.err);
+        if (!ok) break;
+      }
       // scaled scores (log2 units); keys past this row's position are masked out
       const int lim = pos - j * C::TN;
       float mp[8];
