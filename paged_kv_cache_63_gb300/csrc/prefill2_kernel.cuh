@@ -327,26 +327,35 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
           ok = pipe_wait(bar(kB2Full + ik % C::kSlots), (ik / C::kSlots) & 1, abort_flag, a.err);
         if (!ok) break;
       }
-      // scaled scores (log2 units); keys past this row's position are masked out
+      // keys past this row's position are masked out (on tiles that reach the diagonal); the
+      // row maximum of the scaled scores is the extreme raw score times the scale (the
+      // maximum for a non-negative scale, else the minimum), which saves a multiply per score
       const int lim = pos - j * C::TN;
       float mp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-      if (lim >= C::TN - 1) {
+      // warp-uniform: the exponent pass below holds tcgen05.st, which the whole warp executes
+      const bool full = __all_sync(0xffffffffu, lim >= C::TN - 1);
+      float ext;
+      if (sl2 >= 0.f) {
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < C::TN; ++c) {
-          v[c] *= sl2;
-          mp[c & 7] = fmaxf(mp[c & 7], v[c]);
+          for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], v[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], c <= lim ? v[c] : -INFINITY);
         }
+        ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       } else {
 #pragma unroll
-        for (int c = 0; c < C::TN; ++c) {
-          v[c] = c <= lim ? v[c] * sl2 : -INFINITY;
-          mp[c & 7] = fmaxf(mp[c & 7], v[c]);
-        }
+        for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
+#pragma unroll
+        for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? v[c] : INFINITY);
+        ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
+                    fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const float mx = ext * sl2;
       const bool grow = mx > m + kPrefillRescaleSlack;
       if (__any_sync(0xffffffffu, grow)) {
         const float mnew = grow ? mx : m;
@@ -365,23 +374,42 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
         }
         m = mnew;
       }
-      // P = exp2(s - m) as fp16 pairs over the first 64 columns of S
+      // P = exp2(s * scale * log2e - m) as fp16 pairs over the first 64 columns of S (the
+      // scale is folded into one FFMA per score; masked keys give exactly 0)
       float rp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rp[e] = 0.f;
+      const float nm = -m;
+      if (full) {
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float pk[32];
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = h2 * 64 + 2 * e;
-          const float p0 = prefill_exp2(v[c] - m);
-          const float p1 = prefill_exp2(v[c + 1] - m);
-          rp[(2 * e) & 7] += p0;
-          rp[(2 * e + 1) & 7] += p1;
-          pk[e] = __uint_as_float(pack_half2(p0, p1));
+          for (int e = 0; e < 32; ++e) {
+            const int c = h2 * 64 + 2 * e;
+            const float p0 = prefill_exp2(fmaf(v[c], sl2, nm));
+            const float p1 = prefill_exp2(fmaf(v[c + 1], sl2, nm));
+            rp[(2 * e) & 7] += p0;
+            rp[(2 * e + 1) & 7] += p1;
+            pk[e] = __uint_as_float(pack_half2(p0, p1));
+          }
+          tmem_st32(ts + h2 * 32, pk);
         }
-        tmem_st32(ts + h2 * 32, pk);
+      } else {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int c = h2 * 64 + 2 * e;
+            const float p0 = c <= lim ? prefill_exp2(fmaf(v[c], sl2, nm)) : 0.f;
+            const float p1 = c + 1 <= lim ? prefill_exp2(fmaf(v[c + 1], sl2, nm)) : 0.f;
+            rp[(2 * e) & 7] += p0;
+            rp[(2 * e + 1) & 7] += p1;
+            pk[e] = __uint_as_float(pack_half2(p0, p1));
+          }
+          tmem_st32(ts + h2 * 32, pk);
+        }
       }
       l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       tmem_wait_st();

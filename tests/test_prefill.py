@@ -110,6 +110,17 @@ def test_prefill_rescale_path():
     assert_close(got, oracle.prefill(p.cache, p.query, p.query_start), "rescale")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.07])
+def test_prefill_zero_and_negative_scale(scale):
+    """A zero scale averages V over the visible keys; a negative one flips the softmax (the
+    row maximum then comes from the smallest raw score)."""
+    p = CASES["gqa4_ragged"]()
+    p = dataclasses.replace(p, cache=dataclasses.replace(p.cache, scale=scale))
+    got, _ = gpu_prefill(p)
+    assert_close(got, oracle.prefill(p.cache, p.query, p.query_start, scale=scale),
+                 f"scale {scale}")
+
+
 def test_prefill_one_token_matches_decode():
     """One new token per sequence gives the decode step's result (both through the GPU)."""
     from tests.gpu_util import run
