@@ -387,10 +387,15 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int c = h2 * 64 + 2 * e;
-            const float p0 = prefill_exp2(fmaf(v[c], sl2, nm));
-            const float p1 = prefill_exp2(fmaf(v[c + 1], sl2, nm));
-            rp[(2 * e) & 7] += p0;
-            rp[(2 * e + 1) & 7] += p1;
+            // packed fp32 pairs: one FFMA2 for both exponents, one FADD2 for both sums
+            const float2 xx =
+                ffma2(make_float2(v[c], v[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+            const float p0 = prefill_exp2(xx.x);
+            const float p1 = prefill_exp2(xx.y);
+            const float2 acc =
+                fadd2(make_float2(rp[(2 * e) & 7], rp[(2 * e + 1) & 7]), make_float2(p0, p1));
+            rp[(2 * e) & 7] = acc.x;
+            rp[(2 * e + 1) & 7] = acc.y;
             pk[e] = __uint_as_float(pack_half2(p0, p1));
           }
           tmem_st32(ts + h2 * 32, pk);
