@@ -142,6 +142,29 @@ def test_decode_validates_before_touching_a_gpu():
     assert lib.status_of(lib.pa_decode, lib.problem(0, 4, 2, 64, 16, 8, 16), *args) == 0
 
 
+def test_prefill_validates_before_touching_a_gpu():
+    """pa_prefill refuses bad arguments with a status before any device work; valid ones fail
+    only at device lookup here."""
+    prob = P()
+    good = 1 << 20
+    # query, query_start, total_tokens, max_query_len, k, v, bt, ctx, scale, out
+    args = [good, good, 100, 50, good, good, good, good, 0.1, good]
+    assert lib.status_of(lib.pa_prefill, prob, *args) in (5, 6)
+    for i, bad_value, status in [(0, None, 1), (1, None, 1), (2, -1, 1), (3, -1, 1),
+                                 (8, float("inf"), 1), (0, good + 8, 3), (9, good + 4, 3),
+                                 (1, good + 2, 3)]:
+        bad = list(args)
+        bad[i] = bad_value
+        assert lib.status_of(lib.pa_prefill, prob, *bad) == status, (i, bad_value)
+    assert lib.status_of(lib.pa_prefill, P(head_dim=80), *args) == 2
+    assert lib.status_of(lib.pa_prefill, prob, *args, lib.options(stages=2)) == 1
+    # nothing to do is not an error
+    assert lib.status_of(lib.pa_prefill, lib.problem(0, 4, 2, 64, 16, 8, 16), *args) == 0
+    zero_tokens = list(args)
+    zero_tokens[2] = 0
+    assert lib.status_of(lib.pa_prefill, prob, *zero_tokens) == 0
+
+
 def test_schedule_arithmetic(tmp_path):
     """The balanced schedule's tile split (internal.h): every tile of every unit belongs to
     exactly one worker, worker_of inverts worker_start, and slots are unique per
