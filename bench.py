@@ -326,14 +326,24 @@ def cpu_baseline(w, seconds: float) -> dict:
     rng = np.random.default_rng(7)
     seqs = np.sort(rng.choice(w.batch, size=n_seq, replace=False))
     rows = np.concatenate([np.arange(b * g, (b + 1) * g) for b in seqs])
+    cores = oracle.max_threads()
     t0 = time.perf_counter()
     oracle.decode(w, rows=rows)
     dt = time.perf_counter() - t0
     kv = int(w.context_lengths[seqs].astype(np.int64).sum()) * w.kv_heads * w.head_dim * 4
-    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+    # the same oracle on one core, over the calibration sequence alone (then all cores again)
+    t0 = time.perf_counter()
+    oracle.decode(w, rows=np.arange(b0 * g, (b0 + 1) * g), threads=1)
+    dt1 = max(time.perf_counter() - t0, 1e-6)
+    oracle.decode(w, rows=np.arange(b0 * g, b0 * g + 1), threads=cores)
+    kv1 = int(w.context_lengths[b0]) * w.kv_heads * w.head_dim * 4
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{n_seq} of {w.batch} sequences (all {g} query heads each), "
-                      f"{kv / 1e6:.1f} MB of K/V, {dt:.2f} s"}
+                      f"{kv / 1e6:.1f} MB of K/V, {dt:.2f} s",
+            "single_core": {"value": kv1 / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"sequence {b0} ({int(w.context_lengths[b0])} tokens, "
+                                      f"all {g} query heads), {dt1:.2f} s"}}
 
 
 def config_of(w, plan, extra=None):
