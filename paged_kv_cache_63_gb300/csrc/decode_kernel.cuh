@@ -788,6 +788,21 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   // a combine kernel launched as this grid's programmatic dependent may start now; it
   // waits for this grid's completion before reading anything
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  {
+    // warm L2 with the small inputs every warp reads first: the context lengths, the block
+    // table and the queries, one 128-byte line per lane of the grid (no registers held)
+    const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long ctx_lines = (static_cast<long long>(a.batch) * 4 + 127) / 128;
+    const long long bt_lines = (static_cast<long long>(a.batch) * a.maxp * 4 + 127) / 128;
+    const long long q_lines = (static_cast<long long>(a.batch) * a.qh * a.hd * 2 + 127) / 128;
+    for (long long i = tid; i < ctx_lines + bt_lines + q_lines; i += nthreads) {
+      const char *p = i < ctx_lines ? reinterpret_cast<const char *>(a.ctx) + i * 128
+                    : i < ctx_lines + bt_lines ? reinterpret_cast<const char *>(a.bt) + (i - ctx_lines) * 128
+                    : reinterpret_cast<const char *>(a.q) + (i - ctx_lines - bt_lines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+  }
 
   // ---- the worker's range
   Cursor c;
