@@ -293,7 +293,8 @@ def prefill_lines(torch, lib, steps):
                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
                                   "unit": "TFLOP/s", "frac": round(tf / peak, 4),
                                   "peak_source": f"{kind} (bf16 GEMM burst; fp16 same rate)",
-                                  "kernel": "pa::prefill_kernel"}}
+                                  "kernel": ("pa::prefill2_kernel" if p.cache.head_dim <= 128
+                                             else "pa::prefill_kernel")}}
         torch.cuda.empty_cache()
     return res
 
