@@ -2,8 +2,10 @@
 """Benchmark of one paged decode step (libpagedattn.pa_decode) on GB300.
 
 A bench step is one pa_decode call over the whole batch of the named workload (inputs
-resident in HBM), with L2 flushed (a 256 MiB write) before every step, outside the timed
-interval. Prints one JSON line (rank 0): KV-cache read GB/s, microseconds per call, the
+resident in HBM), with L2 flushed before every step, outside the timed interval: a 256 MiB
+write evicts every line, then a 256 MiB read replaces the write's dirty lines with clean
+ones, so the timed kernel neither finds its inputs in L2 nor pays for the flush's own
+write-back. Prints one JSON line (rank 0): KV-cache read GB/s, microseconds per call, the
 roofline of the decode kernel against the measured HBM copy bandwidth, SM clocks sampled
 during the timed region, an end-to-end figure through the C ABI with the per-step inputs
 copied from pinned host memory, and the CPU oracle timed on the host cores.
@@ -35,6 +37,22 @@ DEFAULT_WORKLOAD = "gqa4_mid"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+L2_FLUSH_NOTE = ("flushed before every step, outside the timed interval: 256 MiB write, then a "
+                 "256 MiB read so the write's dirty lines are written back before the interval")
+
+
+class L2Flush:
+    """Evicts L2 (129 MB on GB300) between timed steps. The write alone would leave L2 full
+    of dirty lines whose write-back then lands inside the next timed kernel; the read after
+    it turns them into clean lines of a buffer no kernel under test touches."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 KERNEL_SOURCES = ["device_common.cuh", "decode_kernel.cuh", "decode_launch.cuh", "internal.h",
                   "api.cpp", "launch.cu"]
 
@@ -173,7 +191,7 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
     n = lib.pa_workspace_size(prob, opts)
     ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
     lib.pa_workspace_init(ws, n)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     stream = torch.cuda.current_stream()
     host = None
     if e2e:
@@ -206,7 +224,7 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
                          ws if n else None, n, stream.cuda_stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -220,7 +238,7 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
         sampler.__enter__()
     t0 = time.perf_counter()
     for i in range(steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -252,7 +270,7 @@ def time_prefill(p, steps, warmup, torch, lib):
     d = [torch.from_numpy(x).cuda() for x in (p.query, p.query_start, w.key_cache, w.value_cache,
                                                w.block_tables, w.context_lengths)]
     out = torch.empty((p.total, w.query_heads, w.head_dim), dtype=torch.float32, device="cuda")
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     prob = lib.problem_of(w)
     stream = torch.cuda.current_stream()
 
@@ -261,13 +279,13 @@ def time_prefill(p, steps, warmup, torch, lib):
                        w.scale, out, None, stream.cuda_stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush.zero_()
+        flush()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -352,7 +370,7 @@ def config_of(w, plan, extra=None):
          "kv_heads": w.kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
          "max_pages_per_sequence": w.max_pages_per_sequence,
          "context_tokens": int(w.context_lengths.sum()),
-         "l2": "flushed before every step (256 MiB write, outside the timed interval)",
+         "l2": L2_FLUSH_NOTE,
          "schedule": ["auto", "single", "balanced"][plan["schedule"]],
          "math": ["auto", "simt", "mma"][plan["math"]],
          "workers": plan["workers"], "stages": plan["stages"],

@@ -475,7 +475,10 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
                     static_cast<size_t>(pl.smem_bytes), stream) != cudaSuccess)
     return PA_ERR_CUDA;
   if (a.mode == MODE_BALANCED && !a.fused) {
-    if (launch_combine_balanced(a, pl.units, r.nh_unit, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_combine_balanced(a, pl.units, r.nh_unit,
+                                combine_warps_per_pair(pl.units, pl.workers),
+                                stream) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
   return PA_OK;
 }

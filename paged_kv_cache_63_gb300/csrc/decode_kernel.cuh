@@ -990,76 +990,120 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   finish_unit();
 }
 
-// Separate log-sum-exp combine for the balanced schedule: one CTA of 8 warps per (unit,
-// head), for units shared by many workers. It is launched as a programmatic dependent of
-// the decode kernel, so its CTAs are resident before the decode finishes and start the
-// moment the decode's writes are visible (griddepcontrol.wait). Two passes as in
-// merge_balanced: the maximum over contributors, then the weighted sums; warp w takes
-// contributors w, w + 8, ... and the 8 partial sums are added in warp order.
-template <int HD>
-__global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant__ KernelArgs a) {
+// Separate log-sum-exp combine for the balanced schedule, for units shared by several
+// workers. W warps (W = 1, 2, 4 or 8) merge one (unit, head) pair, so a CTA of 8 warps
+// serves 8 / W pairs: with few contributors per unit one warp per pair keeps the grid to one
+// wave that is resident beside the decode kernel (a programmatic dependent launch: its CTAs
+// come up while the decode runs and start the moment the decode's writes are visible, at
+// griddepcontrol.wait); with tens of contributors W warps share them. Two passes as in
+// merge_balanced: the maximum over contributors, then the weighted sums. Warp `sub` of a
+// pair takes contributors sub, sub + W, ...; a lane holds one contributor's (m, l) of each
+// chunk of 32 and the warp walks the chunk with its weights broadcast by shuffles, so the
+// accumulator loads of a chunk are independent of each other. The W partial sums are added
+// in warp order.
+template <int HD, int W>
+__global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant__ KernelArgs a,
+                                                           int heads, long long pairs) {
+  static_assert(W == 1 || W == 2 || W == 4 || W == 8, "warps per pair");
   constexpr int DPL = HD / 32;
+  constexpr int P = 8 / W;  // pairs per CTA
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const long long unit = blockIdx.x;
-  const int h = blockIdx.y;
-  const int c0 = a.ws_info[2 * unit];
-  const int n = a.ws_info[2 * unit + 1];
-  // entries left by a call that did not finish are skipped, never followed out of range
-  if (n <= 1 || c0 < 0 || n > a.workers || c0 > a.workers - n) return;
-  const UnitInfo u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
-  if (h >= u.nh) return;
-  __shared__ float s_max[8];
-  __shared__ float s_l[8];
-  __shared__ __align__(16) float s_acc[8][HD];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  float mx = -INFINITY;
-  for (int k = tid; k < n; k += 256) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-        a.ws_ml + (slot_of(unit, c0 + k, a.group) * kMaxHeads + h) * 2));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = warp % W;
+  const long long pair = static_cast<long long>(blockIdx.x) * P + warp / W;
+  long long unit = 0;
+  int h = 0, c0 = 0, n = 0;
+  UnitInfo u = {0, 0, 0, 0};
+  if (pair < pairs) {
+    unit = pair / heads;
+    h = static_cast<int>(pair % heads);
+    c0 = a.ws_info[2 * unit];
+    n = a.ws_info[2 * unit + 1];
+    // units finalised by their only worker need nothing; entries left by a call that did
+    // not finish are skipped, never followed out of range
+    if (n <= 1 || c0 < 0 || n > a.workers || c0 > a.workers - n) n = 0;
+    if (n) {
+      u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
+      if (h >= u.nh) n = 0;
+    }
+  }
+  if constexpr (W == 1) {
+    if (n == 0) return;  // no barrier below for a warp per pair
+  }
+  // contributors of this warp: sub, sub + W, ... < n
+  const int mine = n > sub ? (n - sub + W - 1) / W : 0;
+  auto ml_of = [&](int j) {
+    const long long slot = slot_of(unit, c0 + sub + W * j, a.group);
+    return __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
+  };
+  float2 first = make_float2(-INFINITY, 0.f);  // (m, l) of contributor `lane`, kept for pass 2
+  if (lane < mine) first = ml_of(lane);
+  float mx = first.y > 0.f ? first.x : -INFINITY;
+  for (int j = lane + 32; j < mine; j += 32) {
+    const float2 ml = ml_of(j);
     if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) s_max[warp] = mx;
-  __syncthreads();
-  float M = s_max[0];
+  __shared__ float s_max[8];
+  __shared__ float s_l[8];
+  __shared__ __align__(16) float s_acc[W > 1 ? 8 : 1][HD];
+  float M = mx;
+  if constexpr (W > 1) {
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    M = s_max[warp - sub];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_max[w]);
+    for (int w = 1; w < W; ++w) M = fmaxf(M, s_max[warp - sub + w]);
+  }
   float O[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) O[i] = 0.f;
   float L = 0.f;
-#pragma unroll 2
-  for (int k = warp; k < n; k += 8) {
-    const long long slot = slot_of(unit, c0 + k, a.group);
-    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
-    const float w = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
-    L += w * ml.y;
-    const float *src = a.ws_acc + (slot * kMaxHeads + h) * HD + lane * DPL;
+  for (int j0 = 0; j0 < mine; j0 += 32) {
+    float2 ml = first;
+    if (j0 > 0) ml = j0 + lane < mine ? ml_of(j0 + lane) : make_float2(-INFINITY, 0.f);
+    const float wk = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+    L += wk * ml.y;
+    const int cnt = min(32, mine - j0);
+    const float *base = a.ws_acc + static_cast<long long>(h) * HD + lane * DPL;
+#pragma unroll 8
+    for (int t = 0; t < cnt; ++t) {
+      const float w = __shfl_sync(0xffffffffu, wk, t);
+      const float *src = base + slot_of(unit, c0 + sub + W * (j0 + t), a.group) * kMaxHeads * HD;
 #pragma unroll
-    for (int i = 0; i < DPL; i += 2) {
-      const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
-      O[i] += w * v.x;
-      O[i + 1] += w * v.y;
+      for (int i = 0; i < DPL; i += 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
+        O[i] += w * v.x;
+        O[i + 1] += w * v.y;
+      }
     }
   }
 #pragma unroll
-  for (int i = 0; i < DPL; ++i) s_acc[warp][lane * DPL + i] = O[i];
-  if (lane == 0) s_l[warp] = L;
-  __syncthreads();
-  float Lt = 0.f;
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if constexpr (W > 1) {
 #pragma unroll
-  for (int w = 0; w < 8; ++w) Lt += s_l[w];
-  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-  float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0 + h) * HD;
-  for (int d = tid; d < HD; d += 256) {
-    float o = 0.f;
+    for (int i = 0; i < DPL; ++i) s_acc[warp][lane * DPL + i] = O[i];
+    if (lane == 0) s_l[warp] = L;
+    __syncthreads();
+    if (sub != 0) return;
+    L = s_l[warp];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) o += s_acc[w][d];
-    dst[d] = o * inv;
+    for (int i = 0; i < DPL; ++i) O[i] = s_acc[warp][lane * DPL + i];
+#pragma unroll
+    for (int w = 1; w < W; ++w) {
+      L += s_l[warp + w];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) O[i] += s_acc[warp + w][lane * DPL + i];
+    }
   }
+  if (n == 0) return;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float *dst = a.out + (static_cast<long long>(u.b) * a.qh + u.h0 + h) * HD + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; i += 2)
+    *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
 }
 
 // Log-sum-exp combine of the fixed-split arrays: one warp per (sequence, query head).

@@ -86,6 +86,16 @@ PA_HD int64_t worker_of(int64_t x, int64_t total, int64_t workers) {
 // = u + c * group is unique; slots < units + workers * group.
 PA_HD int64_t slot_of(int64_t unit, int64_t worker, int64_t group) { return unit + worker * group; }
 
+// Warps that merge one (unit, head) pair in the separate combine kernel: enough that each
+// walks at most about 8 of the unit's contributors, of which there are 1 + workers / units
+// on average (workers and units both counted in warps).
+inline int combine_warps_per_pair(int64_t units, int64_t workers) {
+  const int64_t avg = 1 + workers / (units > 0 ? units : 1);
+  int w = 1;
+  while (w < 8 && avg > 8 * w) w *= 2;
+  return w;
+}
+
 // ---- launchers (defined in the .cu files) --------------------------------------------
 
 // Tokens per K/V tile for head_dim: `requested` when that size is instantiated, else the
@@ -101,7 +111,8 @@ int simt_heads_instance(int nh);
 cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                           int mma, int nh_inst, int tile, int ctas, int warps_per_cta,
                           size_t smem, cudaStream_t stream);
-cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads,
+// warps_per_pair: 1, 2, 4 or 8 warps merge one (unit, head) pair (combine_warps_per_pair)
+cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads, int warps_per_pair,
                                     cudaStream_t stream);
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);

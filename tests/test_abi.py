@@ -226,6 +226,12 @@ int main() {
       }
     }
   }
+  // warps per (unit, head) pair of the separate combine: at most ~8 contributors per warp
+  const long long wp[][3] = {{256, 1216, 1}, {16, 1216, 8}, {96, 1056, 2}, {96, 1824, 4},
+                             {96, 672, 1}, {96, 768, 2}, {1, 0, 1}, {0, 5, 1}, {4, 100000, 8}};
+  for (const auto &c : wp)
+    if (combine_warps_per_pair(c[0], c[1]) != c[2]) {
+      printf("warps per pair %lld %lld\n", c[0], c[1]); return 1; }
   printf("ok\n");
   return 0;
 }

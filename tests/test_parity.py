@@ -85,6 +85,33 @@ def test_stage_and_warp_options():
     assert lib.status_of(run, w, None, lib.options(stages=8, warps_per_cta=8)) == 2
 
 
+def warps_per_pair(units, workers):
+    """The library's choice of warps per (unit, head) pair in the separate combine kernel:
+    enough that each warp walks at most about 8 of the 1 + workers / units contributors."""
+    avg = 1 + workers // max(units, 1)
+    w = 1
+    while w < 8 and avg > 8 * w:
+        w *= 2
+    return w
+
+
+@pytest.mark.parametrize("avg", [5, 12, 20, 40])
+@pytest.mark.parametrize("name", ["mid_small", "long_small", "g3_hd64_ps8", "g12", "empty_ctx"])
+def test_combine_kernel_warps_per_pair(name, avg):
+    """The separate combine kernel with 1, 2, 4 and 8 warps per (unit, head) pair: worker
+    counts chosen so units have about 5, 12, 20 and 40 contributors."""
+    w, ref = case(name)
+    units = lib.pa_plan(lib.problem_of(w))["units"]
+    o = lib.options(math="mma", schedule="balanced", combine="kernel", workers=units * (avg - 1))
+    pl = lib.pa_plan(lib.problem_of(w), o)
+    assert pl["combine"] == 2
+    assert warps_per_pair(pl["units"], pl["workers"]) == {5: 1, 12: 2, 20: 4, 40: 8}[avg]
+    got = run(w, opts=o)
+    assert_close(got, ref, f"{name}/avg{avg}")
+    assert not got[w.context_lengths == 0].any()
+    assert np.array_equal(got, run(w, opts=o))
+
+
 FULL = ["tiny", "gqa4_mid", "mha", "long_gqa6", "ragged"]
 
 
