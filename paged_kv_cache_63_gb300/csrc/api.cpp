@@ -205,8 +205,8 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
     }
     const int64_t slots = static_cast<int64_t>(units) + pl.workers;
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
-    pl.workspace_bytes = al(int64_t(units) * 4) + al(int64_t(units) * 8) +
-                         al(slots * kMaxHeads * 2 * 4) + al(slots * kMaxHeads * p->head_dim * 4);
+    pl.workspace_bytes = al(int64_t(units) * 4) + al(slots * kMaxHeads * 2 * 4) +
+                         al(slots * kMaxHeads * p->head_dim * 4);
   }
   pl.ctas = ceil_div(std::max(pl.workers, 1), warps);
   return PA_OK;
@@ -455,8 +455,6 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
     char *base = static_cast<char *>(ws);
     a.ws_count = reinterpret_cast<int *>(base);
     base += al(units * 4);
-    a.ws_info = reinterpret_cast<int *>(base);
-    base += al(units * 8);
     a.ws_ml = reinterpret_cast<float *>(base);
     base += al(slots * kMaxHeads * 2 * 4);
     a.ws_acc = reinterpret_cast<float *>(base);
@@ -477,7 +475,7 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
   if (a.mode == MODE_BALANCED && !a.fused) {
     if (launch_combine_balanced(a, pl.units, r.nh_unit,
                                 combine_warps_per_pair(pl.units, pl.workers),
-                                stream) != cudaSuccess)
+                                r.plan.tile_tokens, stream) != cudaSuccess)
       return PA_ERR_CUDA;
   }
   return PA_OK;

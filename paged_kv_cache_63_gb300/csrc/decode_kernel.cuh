@@ -785,9 +785,6 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
   const uint32_t pbuf = qs + NH * HD * 4;           // SIMT: probabilities [T][NHP]
   const uint32_t bar0 = smem_addr(&bars[warp * kMaxStages]);
 
-  // a combine kernel launched as this grid's programmatic dependent may start now; it
-  // waits for this grid's completion before reading anything
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   {
     // warm L2 with the small inputs every warp reads first: the context lengths, the block
     // table and the queries, one 128-byte line per lane of the grid (no registers held)
@@ -820,13 +817,7 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
         const int j = __ffs(empty) - 1;
         empty &= empty - 1;
         const int b = static_cast<int>(base + static_cast<long long>(j) * a.workers);
-        for (int us = member; us < a.ups; us += a.group) {
-          zero_unit<HD>(a, unit_info(a, b, us));
-          if (!a.fused && lane == 0) {
-            a.ws_info[2 * (b * a.ups + us)] = 0;
-            a.ws_info[2 * (b * a.ups + us) + 1] = 0;
-          }
-        }
+        for (int us = member; us < a.ups; us += a.group) zero_unit<HD>(a, unit_info(a, b, us));
       }
     }
     if (!any) return;
@@ -921,10 +912,6 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     const long long c0 = worker_of(cur_ug0, total, nworkers);
     const long long c1 = worker_of(cur_ug0 + nt - 1, total, nworkers);
     const int n = static_cast<int>(c1 - c0 + 1);
-    if (!a.fused && worker == c0 && lane == 0) {
-      a.ws_info[2 * unit] = static_cast<int>(c0);
-      a.ws_info[2 * unit + 1] = n;
-    }
     if (n == 1) {
       Ep::final_out(a, st, cur);
       return;
@@ -981,6 +968,11 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     ++consumed;
     advance(a, c, T);
   }
+  // the combine kernel launched as this grid's programmatic dependent may come up now: its
+  // CTAs prepare during the last warps' tiles and wait for this grid's completion before
+  // reading anything it wrote (triggering at the start instead kept them parked beside the
+  // whole decode, measured slower)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (aborted) {
     // let the copies still in flight land before the shared memory is given up
     for (int i = consumed; i < issued; ++i)
@@ -991,43 +983,63 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
 }
 
 // Separate log-sum-exp combine for the balanced schedule, for units shared by several
-// workers. W warps (W = 1, 2, 4 or 8) merge one (unit, head) pair, so a CTA of 8 warps
-// serves 8 / W pairs: with few contributors per unit one warp per pair keeps the grid to one
-// wave that is resident beside the decode kernel (a programmatic dependent launch: its CTAs
-// come up while the decode runs and start the moment the decode's writes are visible, at
-// griddepcontrol.wait); with tens of contributors W warps share them. Two passes as in
+// workers, launched as a programmatic dependent of the decode kernel. W warps (W = 1, 2, 4
+// or 8) merge one (unit, head) pair, so a CTA of 8 warps serves 8 / W pairs: one warp per
+// pair for a few contributors per unit, W warps sharing tens of them. Its CTAs come up once
+// every decode CTA has finished its tiles (the decode triggers the launch there). Before
+// griddepcontrol.wait, which returns once the decode grid has finished and its writes are
+// visible, a warp reads only inputs: it redoes the decode kernel's balanced split from the
+// context lengths to find its unit's contributors, overlapping the decode's last warps.
+// After it, the contributors' (m, l) and the first batch of accumulators are loaded
+// together, so the merge costs about one memory round trip. Two passes as in
 // merge_balanced: the maximum over contributors, then the weighted sums. Warp `sub` of a
 // pair takes contributors sub, sub + W, ...; a lane holds one contributor's (m, l) of each
-// chunk of 32 and the warp walks the chunk with its weights broadcast by shuffles, so the
-// accumulator loads of a chunk are independent of each other. The W partial sums are added
-// in warp order.
+// chunk of 32 and the warp walks the chunk with its weights broadcast by shuffles, KB
+// accumulator loads in flight at a time. The W partial sums are added in warp order.
 template <int HD, int W>
-__global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant__ KernelArgs a,
-                                                           int heads, long long pairs) {
+__global__ void __launch_bounds__(256)
+    combine_wide_kernel(const __grid_constant__ KernelArgs a, int heads, long long pairs, int T) {
   static_assert(W == 1 || W == 2 || W == 4 || W == 8, "warps per pair");
   constexpr int DPL = HD / 32;
   constexpr int P = 8 / W;  // pairs per CTA
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int KB = HD >= 256 ? 4 : 8;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = warp % W;
   const long long pair = static_cast<long long>(blockIdx.x) * P + warp / W;
-  long long unit = 0;
-  int h = 0, c0 = 0, n = 0;
-  UnitInfo u = {0, 0, 0, 0};
-  if (pair < pairs) {
-    unit = pair / heads;
-    h = static_cast<int>(pair % heads);
-    c0 = a.ws_info[2 * unit];
-    n = a.ws_info[2 * unit + 1];
-    // units finalised by their only worker need nothing; entries left by a call that did
-    // not finish are skipped, never followed out of range
-    if (n <= 1 || c0 < 0 || n > a.workers || c0 > a.workers - n) n = 0;
-    if (n) {
-      u = unit_info(a, static_cast<int>(unit / a.ups), static_cast<int>(unit % a.ups));
-      if (h >= u.nh) n = 0;
-    }
+  const bool valid = pair < pairs;  // warp-uniform
+  const long long unit = valid ? pair / heads : 0;
+  const int h = valid ? static_cast<int>(pair % heads) : 0;
+  const int b = static_cast<int>(unit / a.ups);
+  const int us = static_cast<int>(unit % a.ups);
+  // the decode kernel's split: total tiles over all group units, workers that got tiles, and
+  // the global index of this unit's first tile
+  long long all = 0, before = 0;
+  for (int bb = lane; bb < a.batch; bb += 32) {
+    const long long t = tiles_of(load_ctx(a, bb), T);
+    all += t;
+    if (bb < b) before += t;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    all += __shfl_xor_sync(0xffffffffu, all, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+  }
+  const long long total = all * a.upg;
+  const long long nworkers = total < a.workers ? total : a.workers;
+  const int nt = tiles_of(load_ctx(a, b), T);
+  long long c0 = 0;
+  int n = 0;
+  UnitInfo u = {0, 0, 0, 0};
+  if (valid && nt > 0) {
+    const long long ug0 = before * a.upg + static_cast<long long>(us / a.group) * nt;
+    c0 = worker_of(ug0, total, nworkers);
+    n = static_cast<int>(worker_of(ug0 + nt - 1, total, nworkers) - c0 + 1);
+    u = unit_info(a, b, us);
+    // a unit with one worker was finalised by it; heads past the unit's own do not exist
+    if (n <= 1 || h >= u.nh) n = 0;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if constexpr (W == 1) {
     if (n == 0) return;  // no barrier below for a warp per pair
   }
@@ -1037,8 +1049,26 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant
     const long long slot = slot_of(unit, c0 + sub + W * j, a.group);
     return __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + (slot * kMaxHeads + h) * 2));
   };
-  float2 first = make_float2(-INFINITY, 0.f);  // (m, l) of contributor `lane`, kept for pass 2
+  const float *acc_base = a.ws_acc + static_cast<long long>(h) * HD + lane * DPL;
+  float2 v[KB][DPL / 2];
+  auto load_batch = [&](int j0) {  // accumulators of contributors j0 .. j0 + KB - 1
+#pragma unroll
+    for (int tt = 0; tt < KB; ++tt) {
+      if (j0 + tt < mine) {
+        const float *src =
+            acc_base + slot_of(unit, c0 + sub + W * (j0 + tt), a.group) * kMaxHeads * HD;
+#pragma unroll
+        for (int i = 0; i < DPL / 2; ++i)
+          v[tt][i] = __ldcg(reinterpret_cast<const float2 *>(src + 2 * i));
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL / 2; ++i) v[tt][i] = make_float2(0.f, 0.f);
+      }
+    }
+  };
+  float2 first = make_float2(-INFINITY, 0.f);  // (m, l) of contributor `lane`
   if (lane < mine) first = ml_of(lane);
+  load_batch(0);
   float mx = first.y > 0.f ? first.x : -INFINITY;
   for (int j = lane + 32; j < mine; j += 32) {
     const float2 ml = ml_of(j);
@@ -1067,16 +1097,17 @@ __global__ void __launch_bounds__(256) combine_wide_kernel(const __grid_constant
     const float wk = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
     L += wk * ml.y;
     const int cnt = min(32, mine - j0);
-    const float *base = a.ws_acc + static_cast<long long>(h) * HD + lane * DPL;
-#pragma unroll 8
-    for (int t = 0; t < cnt; ++t) {
-      const float w = __shfl_sync(0xffffffffu, wk, t);
-      const float *src = base + slot_of(unit, c0 + sub + W * (j0 + t), a.group) * kMaxHeads * HD;
+    for (int t0 = 0; t0 < cnt; t0 += KB) {
+      if (j0 + t0 > 0) load_batch(j0 + t0);
 #pragma unroll
-      for (int i = 0; i < DPL; i += 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src + i));
-        O[i] += w * v.x;
-        O[i + 1] += w * v.y;
+      for (int tt = 0; tt < KB; ++tt) {
+        // contributors past the end were loaded as zeros
+        const float w = __shfl_sync(0xffffffffu, wk, (t0 + tt) & 31);
+#pragma unroll
+        for (int i = 0; i < DPL / 2; ++i) {
+          O[2 * i] += w * v[tt][i].x;
+          O[2 * i + 1] += w * v[tt][i].y;
+        }
       }
     }
   }

@@ -60,7 +60,7 @@ cudaError_t launch_decode_hd(const KernelArgs &a, const CUtensorMap *tk, const C
 }
 
 template <int HD, int W>
-cudaError_t launch_combine_balanced_hw(const KernelArgs &a, int units, int heads,
+cudaError_t launch_combine_balanced_hw(const KernelArgs &a, int units, int heads, int tile,
                                        cudaStream_t stream) {
   const long long pairs = static_cast<long long>(units) * heads;
   constexpr int P = 8 / W;
@@ -74,18 +74,18 @@ cudaError_t launch_combine_balanced_hw(const KernelArgs &a, int units, int heads
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_wide_kernel<HD, W>, a, heads, pairs);
+  return cudaLaunchKernelEx(&cfg, combine_wide_kernel<HD, W>, a, heads, pairs, tile);
 }
 
 template <int HD>
 cudaError_t launch_combine_balanced_hd(const KernelArgs &a, int units, int heads,
-                                       int warps_per_pair, cudaStream_t stream) {
+                                       int warps_per_pair, int tile, cudaStream_t stream) {
   if (units == 0 || heads == 0) return cudaSuccess;
   switch (warps_per_pair) {
-    case 1: return launch_combine_balanced_hw<HD, 1>(a, units, heads, stream);
-    case 2: return launch_combine_balanced_hw<HD, 2>(a, units, heads, stream);
-    case 4: return launch_combine_balanced_hw<HD, 4>(a, units, heads, stream);
-    case 8: return launch_combine_balanced_hw<HD, 8>(a, units, heads, stream);
+    case 1: return launch_combine_balanced_hw<HD, 1>(a, units, heads, tile, stream);
+    case 2: return launch_combine_balanced_hw<HD, 2>(a, units, heads, tile, stream);
+    case 4: return launch_combine_balanced_hw<HD, 4>(a, units, heads, tile, stream);
+    case 8: return launch_combine_balanced_hw<HD, 8>(a, units, heads, tile, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -109,8 +109,9 @@ cudaError_t launch_combine_split_hd(const KernelArgs &a, cudaStream_t stream) {
     return launch_decode_hd<HD>(a, tk, tv, mma, nh_inst, tile, ctas, warps, smem, stream);   \
   }                                                                                          \
   cudaError_t launch_combine_balanced_hd##HD(const KernelArgs &a, int units, int heads,      \
-                                             int warps_per_pair, cudaStream_t stream) {      \
-    return launch_combine_balanced_hd<HD>(a, units, heads, warps_per_pair, stream);          \
+                                             int warps_per_pair, int tile,                   \
+                                             cudaStream_t stream) {                          \
+    return launch_combine_balanced_hd<HD>(a, units, heads, warps_per_pair, tile, stream);    \
   }                                                                                          \
   cudaError_t launch_combine_split_hd##HD(const KernelArgs &a, cudaStream_t stream) {        \
     return launch_combine_split_hd<HD>(a, stream);                                           \

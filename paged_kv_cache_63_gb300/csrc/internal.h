@@ -35,7 +35,6 @@ struct KernelArgs {
   float *ws_ml;   // [slots][kMaxHeads][2]  (max in base-2 units, sum)
   float *ws_acc;  // [slots][kMaxHeads][head_dim]
   int *ws_count;  // [units]  merge counters, zero between calls
-  int *ws_info;   // [units][2]  {first worker, number of workers} (combine kernel mode)
   // fixed-split partial arrays: [batch][splits][query_heads]([head_dim])
   float *p_max;
   float *p_sum;
@@ -111,9 +110,10 @@ int simt_heads_instance(int nh);
 cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUtensorMap *tv,
                           int mma, int nh_inst, int tile, int ctas, int warps_per_cta,
                           size_t smem, cudaStream_t stream);
-// warps_per_pair: 1, 2, 4 or 8 warps merge one (unit, head) pair (combine_warps_per_pair)
+// warps_per_pair: 1, 2, 4 or 8 warps merge one (unit, head) pair (combine_warps_per_pair);
+// tile: the decode launch's tokens per tile (the combine redoes its split)
 cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads, int warps_per_pair,
-                                    cudaStream_t stream);
+                                    int tile, cudaStream_t stream);
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
 unsigned *device_error_word();

@@ -11,9 +11,9 @@ cudaError_t launch_decode_hd128(const KernelArgs &, const CUtensorMap *, const C
                                 int, int, int, int, size_t, cudaStream_t);
 cudaError_t launch_decode_hd256(const KernelArgs &, const CUtensorMap *, const CUtensorMap *, int,
                                 int, int, int, int, size_t, cudaStream_t);
-cudaError_t launch_combine_balanced_hd64(const KernelArgs &, int, int, int, cudaStream_t);
-cudaError_t launch_combine_balanced_hd128(const KernelArgs &, int, int, int, cudaStream_t);
-cudaError_t launch_combine_balanced_hd256(const KernelArgs &, int, int, int, cudaStream_t);
+cudaError_t launch_combine_balanced_hd64(const KernelArgs &, int, int, int, int, cudaStream_t);
+cudaError_t launch_combine_balanced_hd128(const KernelArgs &, int, int, int, int, cudaStream_t);
+cudaError_t launch_combine_balanced_hd256(const KernelArgs &, int, int, int, int, cudaStream_t);
 cudaError_t launch_combine_split_hd64(const KernelArgs &, cudaStream_t);
 cudaError_t launch_combine_split_hd128(const KernelArgs &, cudaStream_t);
 cudaError_t launch_combine_split_hd256(const KernelArgs &, cudaStream_t);
@@ -66,11 +66,11 @@ cudaError_t launch_decode(const KernelArgs &a, const CUtensorMap *tk, const CUte
 }
 
 cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads, int warps_per_pair,
-                                    cudaStream_t stream) {
+                                    int tile, cudaStream_t stream) {
   switch (a.hd) {
-    case 64: return launch_combine_balanced_hd64(a, units, heads, warps_per_pair, stream);
-    case 128: return launch_combine_balanced_hd128(a, units, heads, warps_per_pair, stream);
-    case 256: return launch_combine_balanced_hd256(a, units, heads, warps_per_pair, stream);
+    case 64: return launch_combine_balanced_hd64(a, units, heads, warps_per_pair, tile, stream);
+    case 128: return launch_combine_balanced_hd128(a, units, heads, warps_per_pair, tile, stream);
+    case 256: return launch_combine_balanced_hd256(a, units, heads, warps_per_pair, tile, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -116,7 +116,7 @@ def test_plan_heuristic():
 def test_workspace_bytes_cover_slots():
     pl = lib.pa_plan(P(), lib.options(schedule="balanced", workers=100))
     units = pl["units"]
-    need = (units + 100) * 8 * (128 + 2) * 4 + units * 12
+    need = (units + 100) * 8 * (128 + 2) * 4 + units * 4
     assert pl["workspace_bytes"] >= need
 
 
