@@ -153,10 +153,20 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
   pl.tile_tokens = tile_tokens(p->head_dim, o ? o->tile_tokens : 0);
 
   const int stage_bytes = pl.tile_tokens * p->head_dim * 4;
-  // Measured on GB300: eight warps per SM with 16 KB in flight each (one 16 KB stage, or
-  // two 8 KB ones) saturate HBM for this scattered access pattern; deeper rings only add
-  // queueing.
-  int stages = (o && o->stages) ? o->stages : std::max(1, 16384 / stage_bytes);
+  // Measured on GB300: eight warps per SM with 16 to 24 KB in flight each saturate HBM for
+  // this scattered access pattern (three 8 KB stages shorten the tail of gqa4_mid by ~1 %:
+  // SMs differ in memory latency by ~5 %, and deeper rings narrow the spread); a ring that
+  // costs a warp per SM, or deeper ones, only add queueing.
+  int stages = (o && o->stages) ? o->stages : std::max(1, 24576 / stage_bytes);
+  if (!(o && o->stages)) {
+    const int floor_stages = std::max(1, 16384 / stage_bytes);
+    while (stages > floor_stages &&
+           kDefaultWarps * warp_smem_bytes(p->head_dim, r->mma, r->nh_inst, stages,
+                                           pl.tile_tokens) +
+                   kSmemAlign + kStaticSmem >
+               smem_optin)
+      --stages;
+  }
   int per_warp = warp_smem_bytes(p->head_dim, r->mma, r->nh_inst, stages, pl.tile_tokens);
   // Eight warps per CTA: with all of them on neighbouring K/V heads (group below) their
   // reads of a row cover up to 8 * head_dim * 2 contiguous bytes.
