@@ -442,7 +442,10 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (HBM copy)", "traffic": traffic,
                      "algorithmic_bytes_per_launch": nbytes["total"],
-                     "kernel": "pa::decode_kernel"},
+                     "kernel": "pa::decode_kernel",
+                     "interval": ("CUDA events around each pa_decode_ex call: the decode kernel"
+                                  + (" and its dependent combine kernel" if launches_per_call == 2
+                                     else ""))},
         "clocks": clocks,
         "e2e": {"value": round(kv_all / (e2e_step * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "us_per_call": round(e2e_step * 1e3, 2),
