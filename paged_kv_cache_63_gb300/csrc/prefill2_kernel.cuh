@@ -61,7 +61,8 @@ enum : int {
 template <int HD>
 __global__ void __launch_bounds__(kPrefill2Threads, 1)
     prefill2_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
-                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ CUtensorMap tout) {
   using C = Prefill2Cfg<HD>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars2];
@@ -425,16 +426,53 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
     if (ok && my_nt > 0) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float *dst = a.out + (static_cast<size_t>(q0 + my_tok0 + t) * a.qh + kv * a.g + h) * HD;
+      // This warp's 32 rows are 32 / g whole tokens when g divides 32; when all of them are
+      // new tokens of this sequence they leave by TMA stores, staged in the warp's band of
+      // its query tile's buffer (free: every MMA that read it has completed), 32 columns
+      // (128 bytes) at a time in the 128-byte swizzle. Full-line writes, issued
+      // asynchronously; a warp's stores of 16 bytes per row (the other path) leave half
+      // sectors that L2 first fills from DRAM.
+      const int wtok = a.out_tma ? 32 / a.g : 0;
+      if (a.out_tma && my_tok0 + (rg + 1) * wtok <= n) {
+        fence_proxy_async();  // the MMAs' reads of the buffer before these writes
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        float v[32];
-        tmem_ld32(to + c * 32, v);
-        if (valid) {
+        for (int r0 = 0; r0 < HD / 32; r0 += C::KB) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4 *>(dst + c * 32 + e) =
-                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+          for (int cc = 0; cc < C::KB; ++cc) {
+            float v[32];
+            tmem_ld32(to + (r0 + cc) * 32, v);
+            const uint32_t band = q_tile(x) + cc * (C::kRows * 128) + rg * (32 * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              sts128(band + lane * 128 + ((k ^ (lane & 7)) << 4),
+                     make_uint4(__float_as_uint(v[4 * k] * inv), __float_as_uint(v[4 * k + 1] * inv),
+                                __float_as_uint(v[4 * k + 2] * inv),
+                                __float_as_uint(v[4 * k + 3] * inv)));
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int cc = 0; cc < C::KB; ++cc)
+              tma_store_3d(&tout, q_tile(x) + cc * (C::kRows * 128) + rg * (32 * 128),
+                           (r0 + cc) * 32, kv * a.g, q0 + my_tok0 + rg * wtok);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+          }
+          __syncwarp();
+        }
+      } else {
+        float *dst = a.out + (static_cast<size_t>(q0 + my_tok0 + t) * a.qh + kv * a.g + h) * HD;
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          float v[32];
+          tmem_ld32(to + c * 32, v);
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4 *>(dst + c * 32 + e) =
+                  make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+          }
         }
       }
     }

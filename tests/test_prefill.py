@@ -68,6 +68,11 @@ CASES = {
     "ps256": lambda: make_prefill("prefill_chunked", context_lengths=[600, 300],
                                   new_tokens=[200, 300], page_size=256,
                                   max_pages_per_sequence=4, spare_pages=2),
+    # g 6 with head_dim 128 (21 tokens, 126 of 128 rows; g does not divide a warp's 32 rows,
+    # so every row is stored directly)
+    "g6_hd128": lambda: make_prefill("prefill_chunked", context_lengths=[300, 50],
+                                     new_tokens=[300, 50], query_heads=48, kv_heads=8,
+                                     max_pages_per_sequence=32),
     # g 8 (16 tokens per query tile), hd 128
     "g8": lambda: make_prefill("prefill_chunked", context_lengths=[180, 40],
                                new_tokens=[180, 17], query_heads=64, kv_heads=8,
