@@ -75,6 +75,10 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
   const int kv = blockIdx.x, b = blockIdx.y;
   const int pair = a.n_qtiles - 1 - static_cast<int>(blockIdx.z);  // grid.z counts pairs here
 
+  // the first block-table line (the pages of the first key tiles) heads for L2 while the
+  // sequence's offsets are read: the K producer's first lookups then hit L2
+  if (threadIdx.x == 0)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a.bt + static_cast<size_t>(b) * a.maxp));
   const int q0 = __ldg(a.qs + b), q1 = __ldg(a.qs + b + 1), ctx = __ldg(a.ctx + b);
   const int n = q1 - q0;
   if (ctx < 0 || static_cast<long long>(ctx) > static_cast<long long>(a.maxp) << a.ps_shift) {
