@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-others", action="store_true",
                     help="skip the short per-workload summary of the other workloads")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the multi-token kernel on its workloads (one JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline sample")
     ap.add_argument("--math", default="auto")
@@ -380,6 +382,17 @@ def config_of(w, plan, extra=None):
     return c
 
 
+def run_prefill_only(args):
+    import torch
+
+    from paged_kv_cache_63_gb300 import lib
+
+    torch.cuda.set_device(0)
+    lib.load()
+    print(json.dumps({"prefill": prefill_lines(torch, lib, args.steps),
+                      "steps": args.steps, "l2": L2_FLUSH_NOTE}), flush=True)
+
+
 def run_ours(args):
     import torch
 
@@ -542,6 +555,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        run_prefill_only(args)
     else:
         run_ours(args)
 
