@@ -112,8 +112,9 @@ typedef enum pa_combine_t {
   PA_COMBINE_AUTO = 0,  /* heuristic: KERNEL when workers >= units, else FUSED */
   PA_COMBINE_FUSED = 1, /* the last worker to finish a sequence's head group merges it
                            (one launch per call) */
-  PA_COMBINE_KERNEL = 2 /* a separate log-sum-exp combine kernel, one CTA per (unit, head),
-                           launched as a programmatic dependent of the decode kernel */
+  PA_COMBINE_KERNEL = 2 /* a separate log-sum-exp combine kernel, 1 to 8 warps per (unit,
+                           head) by contributor count, launched as a programmatic dependent
+                           of the decode kernel */
 } pa_combine_t;
 
 typedef struct pa_options_t {

@@ -21,8 +21,8 @@ cudaError_t launch_combine_split_hd256(const KernelArgs &, cudaStream_t);
 // One word per device: PA_DEVERR_* bits raised by the kernels.
 __device__ unsigned g_device_error = 0;
 
-// Tokens per K/V tile. head_dim 128 defaults to 16-token tiles (two 8 KB stages per warp):
-// on GB300 they beat 32-token single-stage tiles by ~2 % on mixed context lengths (less
+// Tokens per K/V tile. head_dim 128 defaults to 16-token tiles (8 KB stages, three per warp
+// by default): on GB300 they beat 32-token tiles by ~2 % on mixed context lengths (less
 // imbalance at the end of the balanced split) and are within 0.5 % elsewhere.
 int tile_tokens(int head_dim, int requested) {
   if (head_dim == 128 && (requested == 16 || requested == 32)) return requested;
