@@ -95,11 +95,40 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def code_of(text: str) -> str:
+    """C/C++/CUDA source without comments, whitespace runs collapsed to one space (string
+    literals kept), so that a comment edit leaves a recorded capture valid while a code
+    change invalidates it."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif c.isspace():
+            if out and out[-1] != " ":
+                out.append(" ")
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out).strip()
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_63_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_63_gb300", "csrc", name)) as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -29,3 +29,15 @@ def test_reference_arm_prints_one_contract_line():
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_hash_ignores_comments_only():
+    """A recorded ncu capture stays attached to the code it measured: comment and layout
+    edits keep the hash, code edits change it."""
+    base = 'int f(int a) {\n  return a + 1;  // one\n}\n/* note */ const char *s = "x // y";\n'
+    assert bench.code_of(base) == bench.code_of(base.replace("// one", "// two"))
+    assert bench.code_of(base) == bench.code_of(base.replace("/* note */", ""))
+    assert bench.code_of(base) == bench.code_of(base.replace("  return", "\n\n    return"))
+    assert bench.code_of(base) != bench.code_of(base.replace("a + 1", "a + 2"))
+    assert bench.code_of(base) != bench.code_of(base.replace('"x // y"', '"x / y"'))
+    assert bench.code_of("a + +b") != bench.code_of("a ++b")
