@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-others", action="store_true",
                     help="skip the short per-workload summary of the other workloads")
+    ap.add_argument("--layout", choices=["token_major", "head_major"], default="token_major",
+                    help="K/V cache layout of the timed workload: [page][slot][kv_head][hd] (the "
+                         "pages') or [page][kv_head][slot][hd]")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the multi-token kernel on its workloads (one JSON line)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -440,6 +443,10 @@ def run_ours(args):
     sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     seed = None if rank == 0 else 1000 + rank  # each rank decodes its own batch
     w = make_workload(args.workload, seed=seed)
+    if args.layout == "head_major":
+        from paged_kv_cache_63_gb300.workloads import to_head_major
+
+        w = to_head_major(w)
     plan = lib.pa_plan(lib.problem_of(w), opts, sm_count)
     d = to_device(w, torch)
     nbytes = algorithmic_bytes(w)
@@ -462,7 +469,8 @@ def run_ours(args):
     achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9  # this GPU's kernel (rank 0)
     kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
     launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 2) else 1
-    traffic = recorded_traffic(w.name)
+    # the recorded captures are of the token-major layout
+    traffic = recorded_traffic(w.name) if args.layout == "token_major" else None
     line = {
         "metric": METRIC,
         "value": round(kv_all / (ms_step * 1e-3) / 1e9, 2),
@@ -479,7 +487,7 @@ def run_ours(args):
         "dtype": "f16",
         "accumulate": "f32",
         "data": "synthetic (seeded numpy draws of the workload's shapes and length mix)",
-        "config": config_of(w, plan, {"kv_bytes": nbytes["kv"]}),
+        "config": config_of(w, plan, {"kv_bytes": nbytes["kv"], "cache_layout": args.layout}),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (HBM copy)", "traffic": traffic,
