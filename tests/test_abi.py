@@ -92,6 +92,16 @@ def test_plan_shared_memory_fits_and_tiles():
             assert 1 <= pl["warps_per_cta"] <= 8 and pl["stages"] >= 1
 
 
+def test_plan_keeps_eight_warps_with_up_to_24_kb_in_flight():
+    """The default ring: 24 KB of K/V per warp (three 8 KB stages) where eight warps still
+    fit, else 16 KB; never fewer than eight warps per CTA for these shapes."""
+    for hd, stages in ((64, 3), (128, 3), (256, 1)):
+        pl = lib.pa_plan(P(head_dim=hd, query_heads=32, kv_heads=8), lib.options(math="mma"))
+        assert pl["warps_per_cta"] == 8
+        assert pl["stages"] == stages
+        assert 16384 <= pl["stages"] * pl["tile_tokens"] * hd * 4 <= 24576
+
+
 def test_plan_heuristic():
     # long contexts on few units: balanced split-K with one full wave of workers
     pl = lib.pa_plan(P(batch=4, query_heads=24, kv_heads=4, head_dim=256, page_size=64,
