@@ -47,12 +47,16 @@ WORKLOADS = {
 
 
 @pytest.mark.parametrize("math_", ["simt", "mma"])
-@pytest.mark.parametrize("ns", [1, 2, 3, 7])
+@pytest.mark.parametrize("ns", [1, 2, 3, 7, "max"])
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_partial_states_and_combine(name, ns, math_):
+    """Splits 1, 2, 3, 7 and the most there can be (one page per split for the longest
+    sequence, so shorter ones end in empty splits)."""
     import oracle
 
     w = WORKLOADS[name]()
+    if ns == "max":
+        ns = max(1, int((-(-w.context_lengths.astype(np.int64) // w.page_size)).max()))
     d, pm, pl, po = partial_gpu(w, ns, math_)
     pm, pl, po = pm.cpu().numpy(), pl.cpu().numpy(), po.cpu().numpy()
     for b in range(w.batch):
