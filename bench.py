@@ -579,7 +579,10 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "query_heads": w.query_heads,
                        "kv_heads": w.kv_heads, "head_dim": w.head_dim,
-                       "page_size": w.page_size, "sample_per_step": desc},
+                       "page_size": w.page_size,
+                       "max_pages_per_sequence": w.max_pages_per_sequence,
+                       "context_tokens": int(w.context_lengths.sum()),
+                       "parallelism": "replicas", "sample_per_step": desc},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
                              "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"each step: {desc}"},

@@ -23,7 +23,12 @@ def test_reference_arm_prints_one_contract_line():
     assert line["higher_is_better"] is True and line["n_gpus"] == 1
     assert line["steps"] == 1 and line["warmup"] == 1
     assert line["value"] > 0 and line["ms_per_step"] > 0
-    assert line["config"]["workload"] == bench.DEFAULT_WORKLOAD
+    cfg = line["config"]
+    assert cfg["workload"] == bench.DEFAULT_WORKLOAD
+    # the same workload keys as the GPU arm's config
+    for key in ("batch", "query_heads", "kv_heads", "head_dim", "page_size",
+                "max_pages_per_sequence", "context_tokens", "parallelism"):
+        assert key in cfg, key
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
     e2e = line["e2e"]
