@@ -2,13 +2,16 @@
 """Benchmark of one paged decode step (libpagedattn.pa_decode) on GB300.
 
 A bench step is one pa_decode call over the whole batch of the named workload (inputs
-resident in HBM), with L2 flushed before every step, outside the timed interval: a 256 MiB
-write evicts every line, then a 256 MiB read replaces the write's dirty lines with clean
-ones, so the timed kernel neither finds its inputs in L2 nor pays for the flush's own
-write-back. Prints one JSON line (rank 0): KV-cache read GB/s, microseconds per call, the
-roofline of the decode kernel against the measured HBM copy bandwidth, SM clocks sampled
-during the timed region, an end-to-end figure through the C ABI with the per-step inputs
-copied from pinned host memory, and the CPU oracle timed on the host cores.
+resident in HBM; default: the ragged serving mix, the largest configuration), with L2
+flushed before every step, outside the timed interval: a 256 MiB write evicts every line,
+then a 256 MiB read replaces the write's dirty lines with clean ones, so the timed kernel
+neither finds its inputs in L2 nor pays for the flush's own write-back. Prints one JSON line
+(rank 0): KV-cache read GB/s, microseconds per call, the roofline of the decode kernel
+against the measured HBM copy bandwidth, SM clocks sampled during the timed region, an
+end-to-end figure through the C ABI with every step's inputs copied from pinned host memory
+and its output copied back, and the CPU oracle timed on the host cores. The other full-size
+decode workloads follow as complete blocks of their own (steps, roofline, clocks, e2e), then
+the multi-token kernel's lines.
 
 ``--impl reference`` times the CPU oracle itself (there is no runnable reference library
 for this method) on the same workload and metric.
@@ -33,7 +36,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and μs per call"
-DEFAULT_WORKLOAD = "gqa4_mid"
+DEFAULT_WORKLOAD = "ragged"
+# the other full-size decode workloads, each measured into a block of its own
+OTHER_WORKLOADS = ("gqa4_mid", "mha", "long_gqa6")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -65,7 +70,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-others", action="store_true",
-                    help="skip the short per-workload summary of the other workloads")
+                    help="skip the blocks of the other decode workloads and the prefill lines")
     ap.add_argument("--layout", choices=["token_major", "head_major"], default="token_major",
                     help="K/V cache layout of the timed workload: [page][slot][kv_head][hd] (the "
                          "pages') or [page][kv_head][slot][hd]")
@@ -219,7 +224,7 @@ def to_device(w, torch):
                                 device="cuda"))
 
 
-def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=False):
+def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None):
     """Per-step CUDA-event times (ms) of pa_decode_ex, L2 flushed before each step."""
     prob = lib.problem_of(w)
     n = lib.pa_workspace_size(prob, opts)
@@ -227,33 +232,8 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
     lib.pa_workspace_init(ws, n)
     flush = L2Flush(torch)
     stream = torch.cuda.current_stream()
-    host = None
-    if e2e:
-        # the step's inputs (q, block table, context lengths) packed in one pinned buffer and
-        # moved by one copy; the device-side views point into the copy's destination
-        parts = [w.query.view(np.uint8).reshape(-1), w.block_tables.view(np.uint8).reshape(-1),
-                 w.context_lengths.view(np.uint8).reshape(-1)]
-        offs, total = [], 0
-        for p in parts:
-            offs.append(total)
-            total += (p.size + 255) // 256 * 256
-        packed = torch.empty(total, dtype=torch.uint8).pin_memory()
-        for p, o in zip(parts, offs):
-            packed[o:o + p.size] = torch.from_numpy(p)
-        dev = torch.empty(total, dtype=torch.uint8, device="cuda")
-        views = dict(q=dev[offs[0]:offs[0] + parts[0].size], bt=dev[offs[1]:offs[1] + parts[1].size],
-                     ctx=dev[offs[2]:offs[2] + parts[2].size])
-        host = dict(packed=packed, dev=dev, views=views,
-                    out=torch.empty(d["out"].shape, dtype=torch.float32).pin_memory())
 
     def step():
-        if e2e:
-            host["dev"].copy_(host["packed"], non_blocking=True)
-            v = host["views"]
-            lib.pa_decode_ex(prob, v["q"], d["k"], d["v"], v["bt"], v["ctx"], w.scale, d["out"],
-                             opts, ws if n else None, n, stream.cuda_stream)
-            host["out"].copy_(d["out"], non_blocking=True)
-            return
         lib.pa_decode_ex(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"], opts,
                          ws if n else None, n, stream.cuda_stream)
 
@@ -285,6 +265,81 @@ def time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=None, e2e=Fal
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     clocks = sampler.summary() if sampler else None
     return ms, wall, clocks
+
+
+def time_e2e(w, d, opts, steps, warmup, torch, lib):
+    """End-to-end throughput through the C ABI with the per-step inputs in pinned host memory:
+    every step copies its query, block table and context lengths host-to-device, decodes, and
+    copies its output back. The copies run on two copy streams and the decode on the compute
+    stream, with two device input/output buffers, so step i's copies overlap the decode of
+    steps i - 1 and i + 1, as a serving loop would run them. Returns (ms per step over the
+    whole pipelined run, ms of one step run alone: upload, decode, download)."""
+    prob = lib.problem_of(w)
+    n = lib.pa_workspace_size(prob, opts)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+    lib.pa_workspace_init(ws, n)
+    parts = [w.query.view(np.uint8).reshape(-1), w.block_tables.view(np.uint8).reshape(-1),
+             w.context_lengths.view(np.uint8).reshape(-1)]
+    offs, total = [], 0
+    for p in parts:
+        offs.append(total)
+        total += (p.size + 255) // 256 * 256
+    packed = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for p, o in zip(parts, offs):
+        packed[o:o + p.size] = torch.from_numpy(p)
+    bufs = []
+    for _ in range(2):
+        dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+        bufs.append(dict(dev=dev, q=dev[offs[0]:offs[0] + parts[0].size],
+                         bt=dev[offs[1]:offs[1] + parts[1].size],
+                         ctx=dev[offs[2]:offs[2] + parts[2].size],
+                         out=torch.empty_like(d["out"]),
+                         host_out=torch.empty(d["out"].shape, dtype=torch.float32).pin_memory(),
+                         uploaded=torch.cuda.Event(), decoded=torch.cuda.Event(),
+                         downloaded=torch.cuda.Event()))
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(count):
+        for b in bufs:  # both buffers free at the start
+            b["decoded"].record(comp)
+            b["downloaded"].record(comp)
+        for i in range(count):
+            b = bufs[i % 2]
+            with torch.cuda.stream(up):
+                up.wait_event(b["decoded"])  # the decode two steps back has read this buffer
+                b["dev"].copy_(packed, non_blocking=True)
+                b["uploaded"].record(up)
+            comp.wait_event(b["uploaded"])
+            comp.wait_event(b["downloaded"])  # its output buffer has been read back
+            lib.pa_decode_ex(prob, b["q"], d["k"], d["v"], b["bt"], b["ctx"], w.scale, b["out"],
+                             opts, ws if n else None, n, comp.cuda_stream)
+            b["decoded"].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(b["decoded"])
+                b["host_out"].copy_(b["out"], non_blocking=True)
+                b["downloaded"].record(down)
+        comp.wait_event(bufs[(count - 1) % 2]["downloaded"])
+        if count > 1:
+            comp.wait_event(bufs[count % 2]["downloaded"])
+
+    run(max(warmup, 2))
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    run(steps)
+    t1.record(comp)
+    torch.cuda.synchronize()
+    pipelined = t0.elapsed_time(t1) / steps
+    serial = []
+    for _ in range(5):
+        torch.cuda.synchronize()
+        t0.record(comp)
+        run(1)
+        t1.record(comp)
+        torch.cuda.synchronize()
+        serial.append(t0.elapsed_time(t1))
+    return pipelined, statistics.median(serial)
 
 
 def measured_tensor_peak():
@@ -425,6 +480,63 @@ def run_prefill_only(args):
                       "steps": args.steps, "l2": L2_FLUSH_NOTE}), flush=True)
 
 
+def measure(w, layout, opts, steps, warmup, e2e_steps, torch, lib, sm_count, sampler_dev):
+    """One workload's complete block: device-timed steps (L2 flushed between them) with the
+    clocks sampled during them, the roofline of that interval, and the pipelined end-to-end
+    figure. Returns (block, ms per step, e2e ms per step, algorithmic bytes)."""
+    plan = lib.pa_plan(lib.problem_of(w), opts, sm_count)
+    d = to_device(w, torch)
+    nbytes = algorithmic_bytes(w)
+    ms, wall, clocks = time_decode(w, d, opts, steps, warmup, torch, lib, sampler_dev=sampler_dev)
+    assert lib.pa_get_device_error() == 0
+    e2e_ms, serial_ms = time_e2e(w, d, opts, e2e_steps, warmup, torch, lib)
+    assert lib.pa_get_device_error() == 0
+    del d
+    torch.cuda.empty_cache()
+    ms_step = sum(ms) / len(ms)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9
+    kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
+    launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 2) else 1
+    # the recorded captures are of the token-major layout
+    traffic = recorded_traffic(w.name) if layout == "token_major" else None
+    block = {
+        "workload": w.name,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_call": round(ms_step * 1e3, 2),
+        "us_per_call_median": round(statistics.median(ms) * 1e3, 2),
+        "value": round(kv_gbs, 2),
+        "unit": "GB/s",
+        "pct_of_hbm_peak": round(100 * kv_gbs / peak, 2),
+        "config": config_of(w, plan, {"kv_bytes": nbytes["kv"], "cache_layout": layout}),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": nbytes["total"],
+                     "kernel": "pa::decode_kernel",
+                     "launches_per_call": launches_per_call,
+                     "interval": ("CUDA events on the launching stream around each pa_decode_ex "
+                                  "call: the decode kernel"
+                                  + (" and its dependent combine kernel" if launches_per_call == 2
+                                     else ", the only launch"))},
+        "clocks": clocks,
+        "e2e": {"value": round(nbytes["kv"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(e2e_ms * 1e3, 2), "steps": e2e_steps,
+                "serial_us_per_step": round(serial_ms * 1e3, 2),
+                "h2d_bytes_per_step": nbytes["h2d"], "d2h_bytes_per_step": nbytes["d2h"],
+                "note": "every step copies its q, block table and context lengths from pinned "
+                        "host memory (one copy) and its output back, through pa_decode_ex; "
+                        "copies on two copy streams with two device buffers overlap the "
+                        "neighbouring steps' decodes; serial_us_per_step is one step alone; the "
+                        "K/V cache is resident state (inputs larger than L2, no flush)"},
+        "gpu_launches": steps * launches_per_call,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    return block, ms_step, e2e_ms, nbytes
+
+
 def run_ours(args):
     import torch
 
@@ -441,36 +553,30 @@ def run_ours(args):
     opts = lib.options(schedule=args.schedule, math=args.math, combine=args.combine,
                        workers=args.workers, stages=args.stages, warps_per_cta=args.warps)
     sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    seed = None if rank == 0 else 1000 + rank  # each rank decodes its own batch
-    w = make_workload(args.workload, seed=seed)
-    if args.layout == "head_major":
-        from paged_kv_cache_63_gb300.workloads import to_head_major
-
-        w = to_head_major(w)
-    plan = lib.pa_plan(lib.problem_of(w), opts, sm_count)
-    d = to_device(w, torch)
-    nbytes = algorithmic_bytes(w)
     dev_index = torch.cuda.current_device()
     phys = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     smi_index = int(phys[dev_index]) if phys and phys[0].strip().isdigit() else dev_index
-    ms, wall, clocks = time_decode(w, d, opts, args.steps, args.warmup, torch, lib,
-                                   sampler_dev=smi_index if rank == 0 else None)
-    assert lib.pa_get_device_error() == 0
-    e2e_ms, _, _ = time_decode(w, d, opts, max(10, args.steps // 4), args.warmup, torch, lib,
-                               e2e=True)
+
+    def workload(name, seed=None):
+        w = make_workload(name, seed=seed)
+        if args.layout == "head_major":
+            from paged_kv_cache_63_gb300.workloads import to_head_major
+
+            w = to_head_major(w)
+        return w
+
+    seed = None if rank == 0 else 1000 + rank  # each rank decodes its own batch
+    w = workload(args.workload, seed)
+    e2e_steps = max(10, args.steps // 4)
+    block, ms_step, e2e_step, nbytes = measure(
+        w, args.layout, opts, args.steps, args.warmup, e2e_steps, torch, lib, sm_count,
+        smi_index if rank == 0 else None)
     (ms_step, e2e_step), (kv_all, total_all) = reduce_over_ranks(
-        torch, "cuda", [sum(ms) / len(ms), sum(e2e_ms) / len(e2e_ms)],
-        [nbytes["kv"], nbytes["total"]])
+        torch, "cuda", [ms_step, e2e_step], [nbytes["kv"], nbytes["total"]])
     if rank != 0:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
         return
-    peak, peak_kind = measured_peak()
-    achieved = nbytes["total"] / (ms_step * 1e-3) / 1e9  # this GPU's kernel (rank 0)
-    kv_gbs = nbytes["kv"] / (ms_step * 1e-3) / 1e9
-    launches_per_call = 2 if (plan["schedule"] == 2 and plan["combine"] == 2) else 1
-    # the recorded captures are of the token-major layout
-    traffic = recorded_traffic(w.name) if args.layout == "token_major" else None
     line = {
         "metric": METRIC,
         "value": round(kv_all / (ms_step * 1e-3) / 1e9, 2),
@@ -479,53 +585,31 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
-        "us_per_call": round(ms_step * 1e3, 2),
-        "pct_of_hbm_peak": round(100 * kv_gbs / peak, 2),
+        "us_per_call": block["us_per_call"],
+        "pct_of_hbm_peak": block["pct_of_hbm_peak"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16",
         "accumulate": "f32",
         "data": "synthetic (seeded numpy draws of the workload's shapes and length mix)",
-        "config": config_of(w, plan, {"kv_bytes": nbytes["kv"], "cache_layout": args.layout}),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} (HBM copy)", "traffic": traffic,
-                     "algorithmic_bytes_per_launch": nbytes["total"],
-                     "kernel": "pa::decode_kernel",
-                     "interval": ("CUDA events around each pa_decode_ex call: the decode kernel"
-                                  + (" and its dependent combine kernel" if launches_per_call == 2
-                                     else ""))},
-        "clocks": clocks,
-        "e2e": {"value": round(kv_all / (e2e_step * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "us_per_call": round(e2e_step * 1e3, 2),
-                "h2d_bytes_per_step": nbytes["h2d"], "d2h_bytes_per_step": nbytes["d2h"],
-                "note": "q, block tables and context lengths copied every step from one pinned host "
-                        "buffer (one copy) and the output copied back; the K/V cache is resident "
-                        "state"},
-        "gpu_launches": args.steps * launches_per_call,
-        "wall_s_timed_region": round(wall, 3),
+        "config": block["config"],
+        "roofline": block["roofline"],
+        "clocks": block["clocks"],
+        "e2e": dict(block["e2e"], value=round(kv_all / (e2e_step * 1e-3) / 1e9, 2)),
+        "gpu_launches": block["gpu_launches"],
+        "wall_s_timed_region": block["wall_s_timed_region"],
     }
-    del d
-    torch.cuda.empty_cache()
     if not args.no_others:
         others = {}
-        for name in ("mha", "long_gqa6", "ragged"):
+        for name in OTHER_WORKLOADS:
             if name == w.name:
                 continue
-            wo = make_workload(name)
-            do = to_device(wo, torch)
-            po = lib.pa_plan(lib.problem_of(wo), opts, sm_count)
-            mso, _, _ = time_decode(wo, do, opts, 200, 10, torch, lib)
-            m = sum(mso) / len(mso)
-            nb = algorithmic_bytes(wo)
-            others[name] = {"us_per_call": round(m * 1e3, 2),
-                            "kv_gbs": round(nb["kv"] / (m * 1e-3) / 1e9, 1),
-                            "frac_of_peak": round(nb["total"] / (m * 1e-3) / 1e9 / peak, 4),
-                            "schedule": ["auto", "single", "balanced"][po["schedule"]],
-                            "workers": po["workers"]}
-            del do
-            torch.cuda.empty_cache()
+            wo = workload(name)
+            steps_o = max(args.steps, 200)
+            others[name], _, _, _ = measure(wo, args.layout, opts, steps_o, max(args.warmup, 3),
+                                            max(10, steps_o // 4), torch, lib, sm_count, smi_index)
+            del wo
         line["other_workloads"] = others
         line["prefill"] = prefill_lines(torch, lib, 20)
     line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

@@ -131,8 +131,8 @@ typedef struct pa_options_t {
 
 /* Test hook for the failure path: every warp's first K/V tile waits for 16 bytes that never
  * arrive, so its bounded wait runs out (after about a second), the call raises
- * PA_DEVERR_TIMEOUT and its outputs are invalid; the device stays usable. A workspace used by
- * such a call must be re-initialised with pa_workspace_init. */
+ * PA_DEVERR_TIMEOUT and its outputs are invalid; the device stays usable, and the workspace
+ * the call used needs no re-initialisation (see pa_workspace_init). */
 #define PA_TEST_EXPIRE_WAITS 1
 
 /* What pa_decode / pa_decode_ex will launch for a problem (filled by pa_plan). */
@@ -164,31 +164,50 @@ pa_status_t pa_plan(const pa_problem_t *problem, const pa_options_t *options, in
                     pa_plan_t *plan);
 
 /* Bytes of device workspace pa_decode_ex needs for `problem` and `options` on the current
- * device (0 for the single-pass schedule). */
+ * device (0 for the single-pass schedule). The workspace holds what the split-K schedule of
+ * "[TIL] Optimizing paged attention", section "V4 (Context-axis parallelism)", writes
+ * between its two phases -- per range the running maximum, the sum and the unnormalised
+ * partial output -- plus one merge counter per (sequence, head group) for the fused merge.
+ * That section leaves the buffer to the calling code; here the caller owns it
+ * (pa_decode_ex), or the library does (pa_decode), or a static array (pa_decode_noalloc). */
 pa_status_t pa_workspace_size(const pa_problem_t *problem, const pa_options_t *options,
                               size_t *bytes);
 
 /* Zero a caller-owned workspace (cudaMemsetAsync on `stream`) and record that it is
- * zero. Call it once for every new buffer (also when a freed buffer's address comes back
- * from the allocator). Between calls the buffer must not be written by anyone else. A
- * completed call leaves the merge counters it used at zero; the library remembers, per
- * buffer address, how many are known to be zero and zeroes only the ones a later call with
- * a larger problem adds (on that call's stream). After a call that raised
- * PA_DEVERR_TIMEOUT, call pa_workspace_init again. */
+ * zero -- the split-K buffer of "[TIL] Optimizing paged attention", section "V4
+ * (Context-axis parallelism)", whose merge counters must start at zero. Call it once for
+ * every new buffer (also when a freed buffer's address comes back from the allocator).
+ * Between calls the buffer must not be written by anyone else. A completed call leaves the
+ * merge counters it used at zero; the library remembers, per buffer address, how many are
+ * known to be zero and zeroes only the ones a later call with a larger problem adds (on
+ * that call's stream). A call whose waits expired (PA_DEVERR_TIMEOUT) also leaves its
+ * counters at zero: a warp that gives up still counts its arrival at every unit it shares;
+ * and once pa_get_device_error has reported the timeout, the next call on every workspace
+ * zeroes its counters again in any case. */
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
-/* One decode step with the heuristic's plan. The split-K workspace, when needed, is
- * owned by the library: one grow-only buffer per device, allocated on first need (the
- * first call that needs it must not be inside stream capture), released at process
- * exit. Calls that use that buffer must not overlap in time on different streams.
- * query/key_cache/value_cache: fp16 device pointers; out: fp32 device pointer. */
+/* One decode step with the heuristic's plan: the operation at the top of this file, as
+ * "[TIL] Optimizing paged attention" defines it in sections "Paged Attention" (one query
+ * token per sequence against its cached K/V) and "Baseline" (block-table gather, GQA head
+ * mapping, scaled dot products, softmax, weighted sum of V; fp32 output). The split-K
+ * workspace, when needed, is owned by the library: one grow-only buffer per device,
+ * allocated on first need (the first call that needs it must not be inside stream
+ * capture), released at process exit. Calls that use that buffer must not overlap in time
+ * on different streams. query/key_cache/value_cache: fp16 device pointers; out: fp32
+ * device pointer. Returns PA_OK once the work is queued on `stream`; host-side errors are
+ * returned before anything is queued. */
 pa_status_t pa_decode(const pa_problem_t *problem, const void *query, const void *key_cache,
                       const void *value_cache, const int32_t *block_tables,
                       const int32_t *context_lengths, float scale, float *out, void *stream);
 
 /* pa_decode with explicit options and a caller-owned workspace of workspace_bytes
- * (>= pa_workspace_size; zeroed once by pa_workspace_init). workspace may be NULL when
- * the plan needs none. Concurrent calls must use distinct workspaces. */
+ * (>= pa_workspace_size; zeroed once by pa_workspace_init; 256-byte aligned). workspace may
+ * be NULL when the plan needs none; a missing or short one is PA_ERR_WORKSPACE. Same
+ * operation ("[TIL] Optimizing paged attention", sections "Paged Attention" and
+ * "Baseline"); the options choose how the work is split ("V4 (Context-axis
+ * parallelism)": one pass per sequence, or the context cut across workers and merged by
+ * log-sum-exp) and which arithmetic computes the group x token products. Concurrent calls
+ * must use distinct workspaces. */
 pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const void *key_cache,
                          const void *value_cache, const int32_t *block_tables,
                          const int32_t *context_lengths, float scale, float *out,
@@ -289,13 +308,24 @@ pa_status_t pa_prefill(const pa_problem_t *problem, const void *query, const int
                        const pa_options_t *options, void *stream);
 
 /* Read and clear the device error word of the current device (PA_DEVERR_* bits) after
- * the work queued on `stream` finishes. Synchronises `stream`. */
+ * the work queued on `stream` finishes. Synchronises `stream`. The word records the
+ * preconditions of "[TIL] Optimizing paged attention", section "Paged Attention" (a
+ * sequence's needed block-table entries name pages of the pool; its context fits its table
+ * row) that a call found broken, and expired pipeline waits. *flags receives the bits;
+ * PA_ERR_CUDA if the copy or the synchronisation failed.
+ *
+ * The library caches, per device, device addresses it looked up or allocated (this word,
+ * the pa_decode workspace, the pa_decode_noalloc scratch). They belong to the device's
+ * primary context: after cudaDeviceReset, or any other end of that context, they are stale,
+ * so do not reset a device while the library is in use on it. */
 pa_status_t pa_get_device_error(void *stream, uint32_t *flags);
 
-/* Static description of a status code. */
+/* Static description of a status code (library plumbing; the pages' launch functions return
+ * nothing, section "Baseline"). Never NULL. */
 const char *pa_status_string(pa_status_t status);
 
-/* Library version as 10000 * major + 100 * minor + patch. */
+/* Library version as 10000 * major + 100 * minor + patch (library plumbing, no counterpart in
+ * the pages). */
 int32_t pa_version(void);
 
 #ifdef __cplusplus

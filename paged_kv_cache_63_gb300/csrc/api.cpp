@@ -340,6 +340,17 @@ namespace {
 std::mutex g_zero_mu;
 std::unordered_map<uintptr_t, int64_t> g_zero_counters;
 
+}  // namespace
+
+namespace pa {
+void forget_zeroed_workspaces() {
+  std::lock_guard<std::mutex> lk(g_zero_mu);
+  g_zero_counters.clear();
+}
+}  // namespace pa
+
+namespace {
+
 void note_zeroed(const void *ws, size_t bytes) {
   std::lock_guard<std::mutex> lk(g_zero_mu);
   g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = static_cast<int64_t>(bytes / 4);

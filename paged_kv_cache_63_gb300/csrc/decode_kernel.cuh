@@ -539,6 +539,9 @@ __device__ __forceinline__ void mma_tile(MmaState<HD> &st, const MmaLane<HD, T> 
       st.o[nt][1] *= alpha;
     }
   }
+  // The P.V products use the probabilities rounded to fp16, so the row sum adds those same
+  // rounded values: numerator and denominator then weigh every token alike (a constant V
+  // comes back as that constant up to fp32 summation order).
   float psum = 0.f;
   uint32_t pa[NCH][2];
 #pragma unroll
@@ -547,8 +550,9 @@ __device__ __forceinline__ void mma_tile(MmaState<HD> &st, const MmaLane<HD, T> 
     for (int nt = 0; nt < 2; ++nt) {
       const float p0 = fast_exp2(sc[ch][nt][0] - st.m);
       const float p1 = fast_exp2(sc[ch][nt][1] - st.m);
-      psum += p0 + p1;
       pa[ch][nt] = pack_half2(p0, p1);
+      const float2 pr = half2_bits_to_float2(pa[ch][nt]);
+      psum += pr.x + pr.y;
     }
   st.lsum += psum;
 
@@ -977,6 +981,28 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     // let the copies still in flight land before the shared memory is given up
     for (int i = consumed; i < issued; ++i)
       mbar_wait(bar0 + 8 * (i % S), static_cast<uint32_t>((i / S) & 1), a.err);
+    // Fused merge: still count this warp's arrival at the unit in hand and at every later
+    // unit of its range that it shares with other workers, so that each counter reaches its
+    // contributor count and its last arrival resets it to zero. The rows of those units
+    // are invalid (the error word says so), but the next call finds every counter at zero.
+    if (a.mode == MODE_BALANCED && a.fused) {
+      for (;;) {
+        const long long unit = static_cast<long long>(cur.b) * a.ups + cur.us;
+        const int nt = tiles_of(cur_end, T);
+        const long long c0 = worker_of(cur_ug0, total, nworkers);
+        const long long c1 = worker_of(cur_ug0 + nt - 1, total, nworkers);
+        if (c1 > c0 && lane == 0) {
+          if (atomicAdd(a.ws_count + unit, 1) == static_cast<int>(c1 - c0))
+            atomicExch(a.ws_count + unit, 0);
+        }
+        c.left -= nt - c.tok / T;  // the unit's tiles from the current one on
+        if (c.left <= 0) break;
+        next_unit(a, c, T);
+        cur = unit_info(a, c.b, c.us * a.group + member);
+        cur_ug0 = c.ug0;
+        cur_end = c.end;
+      }
+    }
     return;
   }
   finish_unit();

@@ -117,6 +117,10 @@ cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads, i
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
 unsigned *device_error_word();
+// Drop every record of workspace merge counters known to be zero (api.cpp), so that the
+// next call on each workspace zeroes its counters again; called when the error word shows
+// an expired wait.
+void forget_zeroed_workspaces();
 
 }  // namespace pa
 

@@ -2,8 +2,8 @@
 
 Small cases span several K/V tiles with ragged tails, every head-group shape the library
 handles (g = 1, 2, 3, 4, 6, 8, 12), page sizes 8..256 and empty contexts; every case runs
-through both arithmetic variants and every schedule. Full-size workloads are compared on
-sampled rows, which the oracle computes one by one."""
+through both arithmetic variants and every schedule. Full-size workloads run in the
+benchmark's launch configuration (pa_decode's plan) and are compared on every output element."""
 
 import numpy as np
 import pytest
@@ -116,33 +116,24 @@ FULL = ["tiny", "gqa4_mid", "mha", "long_gqa6", "ragged"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    """Full-size workload in the benchmark's launch configuration (pa_decode's plan),
-    checked on sampled rows plus every row of the longest and the shortest sequence."""
+def test_full_size_every_element(name):
+    """Full-size workload in the benchmark's launch configuration (pa_decode's plan): every
+    element of [batch][query_heads][head_dim] against the oracle."""
     import oracle
 
     w = make_workload(name)
     d = to_device(w)
-    got = run(w, d).reshape(-1, w.head_dim)
-    rng = np.random.default_rng(99)
-    nrows = w.batch * w.query_heads
-    rows = set(rng.choice(nrows, size=min(nrows, 48), replace=False).tolist())
-    for b in (int(np.argmax(w.context_lengths)), int(np.argmin(w.context_lengths))):
-        rows.update(range(b * w.query_heads, (b + 1) * w.query_heads))
-    rows = sorted(rows)
-    ref = oracle.decode(w, rows=rows)
-    assert_close(got[rows], ref, name)
-    assert np.isfinite(got).all()
+    got = run(w, d)
+    assert_close(got, oracle.decode(w), name)
     # a second call gives the same bits
-    again = run(w, d).reshape(-1, w.head_dim)
-    assert np.array_equal(got, again)
+    assert np.array_equal(got, run(w, d))
     # sequences of length 1 return their single V row exactly
+    g = w.query_heads // w.kv_heads
     for b in np.nonzero(w.context_lengths == 1)[0]:
         page = w.block_tables[b, 0]
-        g = w.query_heads // w.kv_heads
         for h in range(w.query_heads):
             v = w.value_cache[page, 0, h // g].astype(np.float32)
-            assert np.array_equal(got[b * w.query_heads + h], v)
+            assert np.array_equal(got[b, h], v)
 
 
 HD128 = ["mid_small", "mha_small", "ragged_small", "g12", "ps256"]
@@ -172,11 +163,9 @@ def test_head_major_parity(name, opt):
 
 
 @pytest.mark.parametrize("name", ["gqa4_mid", "mha"])
-def test_head_major_full_size_sampled(name):
+def test_head_major_full_size_every_element(name):
     import oracle
     from paged_kv_cache_63_gb300.workloads import to_head_major
 
     w = to_head_major(make_workload(name))
-    got = run(w).reshape(-1, w.head_dim)
-    rows = sorted(np.random.default_rng(5).choice(w.batch * w.query_heads, 24, replace=False))
-    assert_close(got[rows], oracle.decode(w, rows=rows), name)
+    assert_close(run(w), oracle.decode(w), name)

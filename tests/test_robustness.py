@@ -169,7 +169,8 @@ def test_workspace_follows_shape_changes():
 def test_expired_wait_is_reported_and_device_stays_usable():
     """Failure detection without a fault: under PA_TEST_EXPIRE_WAITS each warp's first tile
     waits for bytes that never come; the bounded wait gives up (about a second), the call
-    raises PA_DEVERR_TIMEOUT, and the next call on the same device is correct."""
+    raises PA_DEVERR_TIMEOUT, and the next call on the same device and workspace (no
+    re-initialisation) is correct."""
     import oracle
 
     t = torch()
@@ -185,9 +186,53 @@ def test_expired_wait_is_reported_and_device_stays_usable():
     t.cuda.synchronize()
     assert lib.pa_get_device_error() & lib.PA_DEVERR_TIMEOUT
     assert lib.pa_get_device_error() == 0  # reading clears it
-    lib.pa_workspace_init(ws, n)
     lib.pa_decode_ex(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"],
                      lib.options(), ws, n)
     t.cuda.synchronize()
     assert lib.pa_get_device_error() == 0
     assert_close(d["out"].cpu().numpy(), oracle.decode(w), "after an expired wait")
+
+
+@pytest.mark.parametrize("case", ["forced_96_workers", "default_plan"])
+def test_expired_wait_leaves_fused_merge_counters_at_zero(case):
+    """With more units than workers the last worker of each shared unit merges it, counted
+    by a per-unit counter in the workspace. Warps whose waits expire must still count their
+    arrivals, so the counters are back at zero when the call ends, and the next call on the
+    same workspace -- without pa_workspace_init and before the error word is read -- is
+    correct; the one after reading the error word too."""
+    import oracle
+
+    t = torch()
+    forced = case == "forced_96_workers"
+    w = make_workload("ragged", batch=48 if forced else 160)
+    d = to_device(w)
+    prob = lib.problem_of(w)
+    kw = dict(schedule="balanced", combine="fused", workers=96) if forced else {}
+    pl = lib.pa_plan(prob, lib.options(**kw),
+                     t.cuda.get_device_properties(0).multi_processor_count)
+    assert pl["combine"] == 1 and pl["units"] > pl["workers"]
+    ref = oracle.decode(w)
+    bad = lib.options(test_flags=lib.PA_TEST_EXPIRE_WAITS, **kw)
+    good = lib.options(**kw)
+    n = lib.pa_workspace_size(prob, good)
+    ws = t.empty(n, dtype=t.uint8, device="cuda")
+    lib.pa_workspace_init(ws, n)
+    args = (prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"])
+    lib.pa_decode_ex(*args, good, ws, n)  # every shared unit merged once
+    t.cuda.synchronize()
+    assert lib.pa_get_device_error() == 0
+    assert_close(d["out"].cpu().numpy(), ref, "before")
+    lib.pa_decode_ex(*args, bad, ws, n)
+    t.cuda.synchronize()
+    counters = ws[:pl["units"] * 4].view(t.int32).cpu().numpy()
+    assert not counters.any(), f"{int((counters != 0).sum())} merge counters left nonzero"
+    d["out"].fill_(float("nan"))
+    lib.pa_decode_ex(*args, good, ws, n)
+    t.cuda.synchronize()
+    assert lib.pa_get_device_error() & lib.PA_DEVERR_TIMEOUT  # the earlier call's flag
+    assert_close(d["out"].cpu().numpy(), ref, "next call, error word not yet read")
+    d["out"].fill_(float("nan"))
+    lib.pa_decode_ex(*args, good, ws, n)
+    t.cuda.synchronize()
+    assert lib.pa_get_device_error() == 0
+    assert_close(d["out"].cpu().numpy(), ref, "after the error word was read")

@@ -16,34 +16,38 @@ from tests.gpu_util import assert_close, to_device, torch
 
 pytestmark = pytest.mark.gpu
 
+# (workload, overrides, merge the default plan picks: 1 = fused in the decode kernel, 2 =
+# separate combine kernel). The fused merge is the path whose counters live in the scratch.
 WORKLOADS = {
-    "gqa4_mid": dict(),
-    "ragged_b64": dict(batch=64),
-    "long_gqa6_short": dict(context_lengths=[20000, 3000, 77, 1]),
-    "tiny": dict(),
+    "gqa4_mid": ("gqa4_mid", dict(), 2),
+    "ragged_b64": ("ragged", dict(batch=64), 2),
+    "ragged_b160": ("ragged", dict(batch=160), 1),
+    "long_gqa6_short": ("long_gqa6", dict(context_lengths=[20000, 3000, 77, 1]), 2),
+    "tiny": ("tiny", dict(), 2),
 }
-
-
-def _workload(key):
-    name = key.split("_b")[0] if key.startswith("ragged") else key.replace("_short", "")
-    return make_workload(name, **WORKLOADS[key])
 
 
 @pytest.mark.parametrize("key", sorted(WORKLOADS))
 def test_noalloc_matches_pa_decode_on_two_calls_in_a_row(key):
+    """Two pa_decode_noalloc calls in a row give pa_decode's bits exactly (same plan, same
+    kernels, deterministic) and match the oracle within the library's tolerance."""
+    import oracle
+
     t = torch()
-    w = _workload(key)
+    name, kw, merge = WORKLOADS[key]
+    w = make_workload(name, **kw)
     prob = lib.problem_of(w)
     sm = t.cuda.get_device_properties(t.cuda.current_device()).multi_processor_count
     plan = lib.pa_plan(prob, None, sm)
     # the heuristic picks split-K here, so the fixed scratch is really used
-    assert plan["schedule"] == 2
+    assert plan["schedule"] == 2 and plan["combine"] == merge
     assert 0 < plan["workspace_bytes"] <= lib.PA_NOALLOC_SCRATCH_BYTES
     d = to_device(w)
     lib.pa_decode(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, d["out"])
     t.cuda.synchronize()
     assert lib.pa_get_device_error() == 0
     want = d["out"].cpu().numpy()
+    ref = oracle.decode(w)
     for call in range(2):
         out = t.full_like(d["out"], float("nan"))
         lib.pa_decode_noalloc(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale, out)
@@ -51,7 +55,8 @@ def test_noalloc_matches_pa_decode_on_two_calls_in_a_row(key):
         assert lib.pa_get_device_error() == 0
         got = out.cpu().numpy()
         assert np.isfinite(got).all()
-        assert_close(got, want, f"{key} call {call}")
+        assert np.array_equal(got, want), f"{key} call {call}: differs from pa_decode"
+        assert_close(got, ref, f"{key} call {call}")
 
 
 def test_noalloc_refuses_plans_larger_than_its_scratch():
