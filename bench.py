@@ -37,6 +37,9 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode attention: KV-read GB/s (% of HBM peak) and μs per call"
 DEFAULT_WORKLOAD = "ragged"
+PREFILL_WORKLOADS = ("prefill_gqa4", "prefill_chunked", "prefill_mha", "prefill_gqa6_hd256")
+# the library's other kernels, each timed alone on a full-size workload by --kernel-case
+KERNEL_CASES = ("append", "split_combine", "prefill_hd256")
 # the other full-size decode workloads, each measured into a block of its own
 OTHER_WORKLOADS = ("gqa4_mid", "mha", "long_gqa6")
 FALLBACK_HBM_GBS = 6800.0
@@ -76,6 +79,12 @@ def parse_args():
                          "pages') or [page][kv_head][slot][hd]")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the multi-token kernel on its workloads (one JSON line)")
+    ap.add_argument("--kernel-case", choices=KERNEL_CASES,
+                    help="time one other library kernel alone on a full-size workload (one JSON "
+                         "line): the K/V append on ragged, the fixed split's partial and combine "
+                         "kernels on long_gqa6, or the head_dim-256 multi-token kernel")
+    ap.add_argument("--splits", type=int, default=64,
+                    help="splits per sequence of the split_combine case")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline sample")
     ap.add_argument("--math", default="auto")
@@ -389,7 +398,7 @@ def prefill_lines(torch, lib, steps):
 
     peak, kind = measured_tensor_peak()
     res = {}
-    for name in ("prefill_gqa4", "prefill_chunked", "prefill_mha"):
+    for name in PREFILL_WORKLOADS:
         p = make_prefill(name)
         ms = time_prefill(p, steps, 5, torch, lib)
         assert lib.pa_get_device_error() == 0
@@ -478,6 +487,109 @@ def run_prefill_only(args):
     lib.load()
     print(json.dumps({"prefill": prefill_lines(torch, lib, args.steps),
                       "steps": args.steps, "l2": L2_FLUSH_NOTE}), flush=True)
+
+
+def time_calls(fns, steps, warmup, torch):
+    """Mean CUDA-event time (ms) of each of `fns` (callables that launch on the current
+    stream), called in order every step, L2 flushed before each step."""
+    flush = L2Flush(torch)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush()
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+          for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        for k, f in enumerate(fns):
+            f()
+            ev[i][k + 1].record(stream)
+    torch.cuda.synchronize()
+    return [sum(e[k].elapsed_time(e[k + 1]) for e in ev) / steps for k in range(len(fns))]
+
+
+def run_kernel_case(args):
+    """One of the library's other kernels on a full-size workload, timed alone: the command
+    its ncu capture runs. Prints one JSON line with microseconds per call and the kernel's
+    roofline (bytes or FLOPs of the call / its CUDA-event time)."""
+    import torch
+
+    from paged_kv_cache_63_gb300 import lib
+    from paged_kv_cache_63_gb300.workloads import make_prefill, make_workload
+
+    torch.cuda.set_device(0)
+    lib.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    hbm, hbm_kind = measured_peak()
+    line = {"kernel_case": args.kernel_case, "steps": args.steps, "warmup": args.warmup,
+            "l2": L2_FLUSH_NOTE}
+    if args.kernel_case == "append":
+        # one new K/V row per (sequence, K/V head) of ragged, written at the last cached
+        # index (context - 1), whose page every table already holds
+        w = make_workload("ragged")
+        prob = lib.problem_of(w)
+        rng = np.random.default_rng(11)
+        shape = (w.batch, w.kv_heads, w.head_dim)
+        nk = torch.from_numpy(rng.standard_normal(shape).astype(np.float16)).cuda()
+        nv = torch.from_numpy(rng.standard_normal(shape).astype(np.float16)).cuda()
+        k, v = torch.from_numpy(w.key_cache).cuda(), torch.from_numpy(w.value_cache).cuda()
+        bt = torch.from_numpy(w.block_tables).cuda()
+        ctx = torch.from_numpy(w.context_lengths - 1).cuda()
+        (ms,) = time_calls([lambda: lib.pa_append_kv(prob, nk, nv, bt, ctx, k, v, stream)],
+                           args.steps, args.warmup, torch)
+        nbytes = 2 * 2 * nk.numel() * 2 + w.batch * 4 * 2  # rows read and written, ctx, bt
+        line.update(workload="ragged", kernel="pa::append_kv_kernel", us_per_call=round(ms * 1e3, 2),
+                    roofline={"bound": "hbm", "achieved": round(nbytes / (ms * 1e-3) / 1e9, 2),
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                              "peak_source": f"{hbm_kind} (HBM copy)",
+                              "algorithmic_bytes_per_launch": nbytes})
+    elif args.kernel_case == "split_combine":
+        # the pages' fixed split: every sequence of long_gqa6 cut into `splits` ranges
+        w = make_workload("long_gqa6")
+        prob = lib.problem_of(w)
+        d = to_device(w, torch)
+        n = args.splits
+        pm = torch.empty((w.batch, n, w.query_heads), dtype=torch.float32, device="cuda")
+        ps = torch.empty_like(pm)
+        po = torch.empty((w.batch, n, w.query_heads, w.head_dim), dtype=torch.float32,
+                         device="cuda")
+        ms_p, ms_c = time_calls(
+            [lambda: lib.pa_split_kv_partial(prob, d["q"], d["k"], d["v"], d["bt"], d["ctx"],
+                                             w.scale, n, pm, ps, po, stream=stream),
+             lambda: lib.pa_split_kv_combine(prob, n, pm, ps, po, d["out"], stream)],
+            args.steps, args.warmup, torch)
+        part = (pm.numel() + ps.numel() + po.numel()) * 4
+        comb = part + d["out"].numel() * 4
+        kv = algorithmic_bytes(w)["total"] + part
+        line.update(workload="long_gqa6", splits=n,
+                    partial={"kernel": "pa::decode_kernel (fixed split)",
+                             "us_per_call": round(ms_p * 1e3, 2),
+                             "achieved": round(kv / (ms_p * 1e-3) / 1e9, 2), "unit": "GB/s",
+                             "frac": round(kv / (ms_p * 1e-3) / 1e9 / hbm, 4)},
+                    kernel="pa::combine_split_kernel", us_per_call=round(ms_c * 1e3, 2),
+                    roofline={"bound": "hbm", "achieved": round(comb / (ms_c * 1e-3) / 1e9, 2),
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": round(comb / (ms_c * 1e-3) / 1e9 / hbm, 4),
+                              "peak_source": f"{hbm_kind} (HBM copy)",
+                              "algorithmic_bytes_per_launch": comb})
+    else:
+        p = make_prefill("prefill_gqa6_hd256")
+        ms = time_prefill(p, args.steps, args.warmup, torch, lib)
+        peak, kind = measured_tensor_peak()
+        flops = 4.0 * p.causal_pairs() * p.cache.query_heads * p.cache.head_dim
+        tf = flops / (ms * 1e-3) / 1e12
+        line.update(workload="prefill_gqa6_hd256", kernel="pa::prefill_kernel<256>",
+                    us_per_call=round(ms * 1e3, 1),
+                    roofline={"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                              "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                              "peak_source": f"{kind} (bf16 GEMM burst; fp16 same rate)",
+                              "causal_flops": flops})
+    assert lib.pa_get_device_error() == 0
+    print(json.dumps(line), flush=True)
 
 
 def measure(w, layout, opts, steps, warmup, e2e_steps, torch, lib, sm_count, sampler_dev):
@@ -681,6 +793,8 @@ def main():
         run_reference(args)
     elif args.prefill_only:
         run_prefill_only(args)
+    elif args.kernel_case:
+        run_kernel_case(args)
     else:
         run_ours(args)
 

@@ -159,6 +159,8 @@ PREFILL_SPECS: Dict[str, tuple] = {
     "prefill_gqa4": ("gqa4_mid", dict(batch=8, context_lengths=[2048] * 8), ("all",)),
     "prefill_chunked": ("gqa4_mid", dict(batch=16), ("last", 512)),
     "prefill_mha": ("mha", dict(batch=8, context_lengths=[2048] * 8), ("all",)),
+    # head_dim 256 (the single-tile kernel): two fresh 4096-token prompts, 24/4 heads, page 64
+    "prefill_gqa6_hd256": ("long_gqa6", dict(batch=2, context_lengths=[4096] * 2), ("all",)),
 }
 
 

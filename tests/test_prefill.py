@@ -140,7 +140,8 @@ def test_prefill_one_token_matches_decode():
     assert np.abs(got - dec).max() < 4e-3
 
 
-@pytest.mark.parametrize("name", ["prefill_gqa4", "prefill_chunked", "prefill_mha"])
+@pytest.mark.parametrize("name", ["prefill_gqa4", "prefill_chunked", "prefill_mha",
+                                  "prefill_gqa6_hd256"])
 def test_prefill_full_size_every_element(name):
     p = make_prefill(name)
     got, _ = gpu_prefill(p)
