@@ -300,23 +300,6 @@ pa_status_t encode_query_map(CUtensorMap *map, const void *query, int64_t total_
   return rc == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status_t encode_out_map(CUtensorMap *map, float *out, int64_t total_tokens, int query_heads,
-                           int head_dim, int heads_per_box, int tokens_per_box) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return PA_ERR_CUDA;
-  const cuuint64_t hd = static_cast<cuuint64_t>(head_dim);
-  cuuint64_t dims[3] = {hd, static_cast<cuuint64_t>(query_heads),
-                        static_cast<cuuint64_t>(total_tokens > 0 ? total_tokens : 1)};
-  cuuint64_t strides[2] = {hd * 4, static_cast<cuuint64_t>(query_heads) * hd * 4};
-  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(heads_per_box),
-                       static_cast<cuuint32_t>(tokens_per_box)};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult rc = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return rc == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
-}
-
 pa_status_t check_problem_public(const pa_problem_t *p) { return check_problem(p); }
 
 pa_status_t current_device_smem(int *smem_optin) {

@@ -1163,41 +1163,79 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
 }
 
-// Log-sum-exp combine of the fixed-split arrays: one warp per (sequence, query head).
+// Log-sum-exp combine of the fixed-split arrays (section "V4 (Context-axis parallelism)"'s
+// merge: empty splits are skipped, the rest rescaled to a common maximum and normalised).
+// One CTA of kCombineSplitWarps warps per (sequence, query head). Every warp first reduces
+// the splits' (max, sum) pairs, 32 splits per round, to the common maximum M and the total
+// L; warp w then adds the accumulator rows of splits w, w + W, w + 2W, ..., each weighted by
+// exp2(m_s - M), with the weights of 32 splits computed at once and the row loads of
+// consecutive splits independent of each other; warp 0 adds the W partial rows in warp order
+// and divides by L. The summation order is fixed, so results are deterministic.
+constexpr int kCombineSplitWarps = 8;
+
 template <int HD>
-__global__ void __launch_bounds__(256) combine_split_kernel(const __grid_constant__ KernelArgs a) {
+__global__ void __launch_bounds__(kCombineSplitWarps * 32)
+    combine_split_kernel(const __grid_constant__ KernelArgs a) {
   constexpr int DPL = HD / 32;
-  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (row >= static_cast<long long>(a.batch) * a.qh) return;
-  const int lane = threadIdx.x & 31;
-  const long long b = row / a.qh;
-  const long long h = row % a.qh;
-  float M = -INFINITY, L = 0.f;
+  constexpr int W = kCombineSplitWarps;
+  __shared__ __align__(16) float part[W][HD];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long b = blockIdx.x / a.qh;
+  const long long h = blockIdx.x % a.qh;
+  const int n = a.num_splits;
+  auto idx_of = [&](int s) { return (b * n + s) * a.qh + h; };
+  float M = -INFINITY;
+  for (int s = lane; s < n; s += 32) {
+    const long long i = idx_of(s);
+    if (__ldg(a.p_sum + i) != 0.f) M = fmaxf(M, __ldg(a.p_max + i));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+  for (int s = lane; s < n; s += 32) {
+    const long long i = idx_of(s);
+    const float l = __ldg(a.p_sum + i);
+    if (l != 0.f) L += fast_exp2(__ldg(a.p_max + i) - M) * l;
+  }
+  L = warp_sum(L);
   float O[DPL];
 #pragma unroll
   for (int i = 0; i < DPL; ++i) O[i] = 0.f;
-  for (int s = 0; s < a.num_splits; ++s) {
-    const long long idx = (b * a.num_splits + s) * a.qh + h;
-    const float l = __ldg(a.p_sum + idx);
-    if (l == 0.f) continue;
-    const float m = __ldg(a.p_max + idx);
-    const float Mn = fmaxf(M, m);
-    const float al = fast_exp2(M - Mn);
-    const float be = fast_exp2(m - Mn);
-    L = al * L + be * l;
-    const float *src = a.p_out + idx * HD + lane * DPL;
-#pragma unroll
-    for (int i = 0; i < DPL; i += 2) {
-      const float2 v = __ldg(reinterpret_cast<const float2 *>(src + i));
-      O[i] = al * O[i] + be * v.x;
-      O[i + 1] = al * O[i + 1] + be * v.y;
+  for (int base = warp; base < n; base += 32 * W) {
+    // lane j weighs split base + j * W (0 for an empty split or one past the end)
+    const int sj = base + lane * W;
+    float wj = 0.f;
+    if (sj < n) {
+      const long long i = idx_of(sj);
+      if (__ldg(a.p_sum + i) != 0.f) wj = fast_exp2(__ldg(a.p_max + i) - M);
     }
-    M = Mn;
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  float *dst = a.out + row * HD + lane * DPL;
+    const int cnt = min(32, (n - base + W - 1) / W);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wt = __shfl_sync(0xffffffffu, wj, j);
+      if (wt == 0.f) continue;
+      const float *src = a.p_out + idx_of(base + j * W) * HD + lane * DPL;
 #pragma unroll
-  for (int i = 0; i < DPL; i += 2) *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
+      for (int i = 0; i < DPL; i += 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2 *>(src + i));
+        O[i] = fmaf(wt, v.x, O[i]);
+        O[i + 1] = fmaf(wt, v.y, O[i + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) part[warp][lane * DPL + i] = O[i];
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int w = 1; w < W; ++w)
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) O[i] += part[w][lane * DPL + i];
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float *dst = a.out + static_cast<long long>(blockIdx.x) * HD + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; i += 2)
+    *reinterpret_cast<float2 *>(dst + i) = make_float2(O[i] * inv, O[i + 1] * inv);
 }
 
 }  // namespace pa

@@ -92,10 +92,10 @@ cudaError_t launch_combine_balanced_hd(const KernelArgs &a, int units, int heads
 
 template <int HD>
 cudaError_t launch_combine_split_hd(const KernelArgs &a, cudaStream_t stream) {
-  const long long threads = static_cast<long long>(a.batch) * a.qh * 32;
-  const int blocks = static_cast<int>((threads + 255) / 256);
+  const long long blocks = static_cast<long long>(a.batch) * a.qh;  // one per (sequence, head)
   if (blocks == 0) return cudaSuccess;
-  combine_split_kernel<HD><<<blocks, 256, 0, stream>>>(a);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  combine_split_kernel<HD><<<static_cast<unsigned>(blocks), kCombineSplitWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -146,10 +146,6 @@ pa_status_t encode_cache_map_rows(CUtensorMap *map, const void *base, const pa_p
                                   int rows_per_box);
 pa_status_t encode_query_map(CUtensorMap *map, const void *query, int64_t total_tokens,
                              int query_heads, int head_dim, int heads_per_box, int tokens_per_box);
-// fp32 [total_tokens][query_heads][head_dim] output as a 3-D TMA store target: box of 32
-// columns x heads_per_box heads x tokens_per_box tokens, 128-byte swizzle.
-pa_status_t encode_out_map(CUtensorMap *map, float *out, int64_t total_tokens, int query_heads,
-                           int head_dim, int heads_per_box, int tokens_per_box);
 pa_status_t check_problem_public(const pa_problem_t *p);
 // The current device's opt-in shared memory per block; PA_ERR_NO_DEVICE unless sm_103.
 pa_status_t current_device_smem(int *smem_optin);

@@ -35,8 +35,7 @@ cudaError_t launch_prefill_hd(const PrefillArgs &a, const CUtensorMap &tq, const
 // head_dim 64 / 128: two query tiles per CTA (a.n_qtiles counts pairs, grid.z too)
 template <int HD>
 cudaError_t launch_prefill2_hd(const PrefillArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                               const CUtensorMap &tv, const CUtensorMap &to, dim3 grid,
-                               cudaStream_t stream) {
+                               const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
   using C = Prefill2Cfg<HD>;
   auto kern = prefill2_kernel<HD>;
   constexpr int smem = C::kSmem + 1024;
@@ -49,7 +48,7 @@ cudaError_t launch_prefill2_hd(const PrefillArgs &a, const CUtensorMap &tq, cons
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevicesPrefill) set[dev] = true;
   }
-  kern<<<grid, kPrefill2Threads, smem, stream>>>(a, tq, tk, tv, to);
+  kern<<<grid, kPrefill2Threads, smem, stream>>>(a, tq, tk, tv);
   return cudaGetLastError();
 }
 
@@ -118,15 +117,11 @@ extern "C" pa_status_t pa_prefill(const pa_problem_t *problem, const void *query
   a.n_qtiles = static_cast<int>(n_qtiles);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.expire = (options && (options->test_flags & PA_TEST_EXPIRE_WAITS)) ? 1 : 0;
-  a.out_tma = (hd != 256 && 32 % g == 0) ? 1 : 0;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
 
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   const int rows = a.ps < tn ? a.ps : tn;
   st = encode_query_map(&tq, query, total_tokens, a.qh, hd, g, qt);
-  if (st != PA_OK) return st;
-  // rows of one softmax warp: 32 / g tokens x g heads, in 32-column (128-byte) pieces
-  st = encode_out_map(&to, out, total_tokens, a.qh, hd, a.out_tma ? g : 1,
-                      a.out_tma ? 32 / g : 1);
   if (st != PA_OK) return st;
   st = encode_cache_map_rows(&tk, key_cache, problem, rows);
   if (st != PA_OK) return st;
@@ -139,10 +134,10 @@ extern "C" pa_status_t pa_prefill(const pa_problem_t *problem, const void *query
   const dim3 grid(a.kvh, a.batch, a.n_qtiles);
   switch (hd) {
     case 64:
-      e = launch_prefill2_hd<64>(a, tq, tk, tv, to, grid, s);
+      e = launch_prefill2_hd<64>(a, tq, tk, tv, grid, s);
       break;
     case 128:
-      e = launch_prefill2_hd<128>(a, tq, tk, tv, to, grid, s);
+      e = launch_prefill2_hd<128>(a, tq, tk, tv, grid, s);
       break;
     case 256:
       e = launch_prefill_hd<256>(a, tq, tk, tv, grid, s);

@@ -37,8 +37,7 @@ struct PrefillArgs {
   float scale_log2;
   int expire;  // PA_TEST_EXPIRE_WAITS: the MMA warp's first wait is on a barrier that
                // completes only at the end, so it runs out
-  int out_tma;  // head_dim 64 / 128 with g dividing 32: rows of a softmax warp leave by TMA
-                // stores (box 32 fp32 x g heads x 32 / g tokens)
+  int out_v8;  // out is 32-byte aligned: the two-tile kernel writes rows in 32-byte stores
 };
 
 template <int HD>
