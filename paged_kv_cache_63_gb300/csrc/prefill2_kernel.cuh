@@ -275,6 +275,10 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
       if (is_v) prefetch_tensormap(&tq);
     }
     const CUtensorMap *map = is_v ? &tv : &tk;
+    // L2 policies: every pair of query tiles of a (sequence, K/V head) reads its K/V tiles,
+    // so they stay (evict last); each Q tile is read once (evict first)
+    const uint64_t pol = l2_evict_last_policy();
+    const uint64_t pol_q = l2_evict_first_policy();
     const int rows_per_box = min(a.ps, C::TN);
     const int boxes = C::TN / rows_per_box;
     const uint32_t box_bytes = rows_per_box * 128;
@@ -299,8 +303,8 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
           for (int x = 0; x < 2; ++x)
 #pragma unroll
             for (int kb = 0; kb < C::KB; ++kb)
-              tma_load_3d_plain(q_tile(x) + kb * (C::kRows * 128), &tq, bar(kB2QFull), kb * 64,
-                                it.kv * a.g, it.q0 + (x ? it.tok0_b : it.tok0_a));
+              tma_load_3d(q_tile(x) + kb * (C::kRows * 128), &tq, bar(kB2QFull), kb * 64,
+                          it.kv * a.g, it.q0 + (x ? it.tok0_b : it.tok0_a), pol_q);
         }
         ++q_loads;
       }
@@ -340,8 +344,8 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
         if (page >= 0) {
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d_plain(slot_addr(s) + kb * (C::TN * 128) + lane * box_bytes, map,
-                              bar(kB2Full + s), kb * 64, y, z);
+            tma_load_3d(slot_addr(s) + kb * (C::TN * 128) + lane * box_bytes, map,
+                        bar(kB2Full + s), kb * 64, y, z, pol);
         }
         last_item = item;
       }

@@ -227,11 +227,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         mbar_arrive_expect_tx(bar(kBarQ), C::KB * q_rows * 128);
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d_plain(sq + kb * (C::kRows * 128), &tq, bar(kBarQ), kb * 64, kv * a.g,
-                            q0 + tok0);
+          tma_load_3d(sq + kb * (C::kRows * 128), &tq, bar(kBarQ), kb * 64, kv * a.g, q0 + tok0,
+                      l2_evict_first_policy());  // read once
       }
     }
     const CUtensorMap *map = is_v ? &tv : &tk;
+    // every query tile of the (sequence, K/V head) reads these K/V tiles: keep them in L2
+    const uint64_t pol = l2_evict_last_policy();
     const int full = is_v ? kBarVFull : kBarKFull;
     const int empty = is_v ? kBarVEmpty : kBarKEmpty;
     const uint32_t stage0 = is_v ? v_stage(0) : k_stage(0);
@@ -274,8 +276,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (page >= 0) {
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d_plain(stage0 + st * C::kKVBytes + kb * (C::TN * 128) + lane * box_bytes, map,
-                            bar(full + st), kb * 64, y, z);
+          tma_load_3d(stage0 + st * C::kKVBytes + kb * (C::TN * 128) + lane * box_bytes, map,
+                      bar(full + st), kb * 64, y, z, pol);
       }
       issued = j + 1;
     }
