@@ -83,13 +83,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
-// L2 policy for bytes that other CTAs read again soon: keep them ahead of streamed data.
-__device__ __forceinline__ uint64_t l2_evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // TMA tiled load of a 3-D box into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
                                             int x, int y, int z, uint64_t policy) {

@@ -78,6 +78,13 @@ enum : int {
   kNumBars = 16
 };
 
+// L2 policy for bytes that other CTAs read again soon: keep them ahead of streamed data.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ float prefill_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
