@@ -110,8 +110,9 @@ typedef enum pa_math_t {
 /* Where the split-K merge runs (balanced schedule). */
 typedef enum pa_combine_t {
   PA_COMBINE_AUTO = 0,  /* heuristic: KERNEL when workers >= units, else FUSED */
-  PA_COMBINE_FUSED = 1, /* the last worker to finish a sequence's head group merges it
-                           (one launch per call) */
+  PA_COMBINE_FUSED = 1, /* the worker holding a sequence's head group's first tiles merges
+                           it once the other workers sharing it have published their
+                           states (one launch per call) */
   PA_COMBINE_KERNEL = 2 /* a separate log-sum-exp combine kernel, 1 to 8 warps per (unit,
                            head) by contributor count, launched as a programmatic dependent
                            of the decode kernel */
@@ -167,23 +168,21 @@ pa_status_t pa_plan(const pa_problem_t *problem, const pa_options_t *options, in
  * device (0 for the single-pass schedule). The workspace holds what the split-K schedule of
  * "[TIL] Optimizing paged attention", section "V4 (Context-axis parallelism)", writes
  * between its two phases -- per range the running maximum, the sum and the unnormalised
- * partial output -- plus one merge counter per (sequence, head group) for the fused merge.
+ * partial output -- plus one flag per range for the fused merge (the range's state is
+ * published by writing the call's number into it).
  * That section leaves the buffer to the calling code; here the caller owns it
  * (pa_decode_ex), or the library does (pa_decode), or a static array (pa_decode_noalloc). */
 pa_status_t pa_workspace_size(const pa_problem_t *problem, const pa_options_t *options,
                               size_t *bytes);
 
-/* Zero a caller-owned workspace (cudaMemsetAsync on `stream`) and record that it is
- * zero -- the split-K buffer of "[TIL] Optimizing paged attention", section "V4
- * (Context-axis parallelism)", whose merge counters must start at zero. Call it once for
- * every new buffer (also when a freed buffer's address comes back from the allocator).
- * Between calls the buffer must not be written by anyone else. A completed call leaves the
- * merge counters it used at zero; the library remembers, per buffer address, how many are
- * known to be zero and zeroes only the ones a later call with a larger problem adds (on
- * that call's stream). A call whose waits expired (PA_DEVERR_TIMEOUT) also leaves its
- * counters at zero: a warp that gives up still counts its arrival at every unit it shares;
- * and once pa_get_device_error has reported the timeout, the next call on every workspace
- * zeroes its counters again in any case. */
+/* Zero a caller-owned workspace (cudaMemsetAsync on `stream`) -- the split-K buffer of
+ * "[TIL] Optimizing paged attention", section "V4 (Context-axis parallelism)". Call it once
+ * for every new buffer (also when a freed buffer's address comes back from the allocator):
+ * the fused merge's flags must not start out holding arbitrary values. Between calls the
+ * buffer must not be written by anyone else. Nothing needs resetting after a call, whether
+ * it completed or its waits expired (PA_DEVERR_TIMEOUT): every call publishes its partial
+ * states under a number of its own (unique within the process, never 0), so flags that
+ * earlier calls left behind never match a later call's. */
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /* One decode step with the heuristic's plan: the operation at the top of this file, as
@@ -231,10 +230,10 @@ pa_status_t pa_decode_ex(const pa_problem_t *problem, const void *query, const v
  *    workspace_bytes) is refused with PA_ERR_WORKSPACE before any launch.
  *  - The first call on each device looks up the array's device address (and may load the
  *    library's GPU code); make that first call before any stream capture begins.
- *  - Every call shares the one array per device and it keeps the previous call's contents;
- *    the merge counters in it are cleared on `stream` at the start of each call. Calls
- *    whose work overlaps on the GPU (other streams, other host threads) race on the array
- *    and give wrong results: serialise them. */
+ *  - Every call shares the one array per device and it keeps the previous call's contents
+ *    (none of it needs clearing: each call publishes its partial states under a number of
+ *    its own). Calls whose work overlaps on the GPU (other streams, other host threads)
+ *    race on the array and give wrong results: serialise them. */
 pa_status_t pa_decode_noalloc(const pa_problem_t *problem, const void *query,
                               const void *key_cache, const void *value_cache,
                               const int32_t *block_tables, const int32_t *context_lengths,

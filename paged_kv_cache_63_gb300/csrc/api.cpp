@@ -4,10 +4,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
-#include <unordered_map>
 
 #include "internal.h"
 #include "pagedattn.h"
@@ -215,7 +215,7 @@ pa_status_t resolve(const pa_problem_t *p, const pa_options_t *o, int sm_count, 
     }
     const int64_t slots = static_cast<int64_t>(units) + pl.workers;
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
-    pl.workspace_bytes = al(int64_t(units) * 4) + al(slots * kMaxHeads * 2 * 4) +
+    pl.workspace_bytes = al(slots * 4) + al(slots * kMaxHeads * 2 * 4) +
                          al(slots * kMaxHeads * p->head_dim * 4);
   }
   pl.ctas = ceil_div(std::max(pl.workers, 1), warps);
@@ -314,47 +314,22 @@ pa_status_t current_device_smem(int *smem_optin) {
 
 namespace {
 
-// ---- merge counters -------------------------------------------------------------------
-// The fused merge keeps one counter per unit at the start of the workspace; a call leaves
-// the counters it used at zero, but its partial states overwrite whatever lies past them.
-// So for every workspace the library remembers how many leading counters are known to be
-// zero, and before a call that needs more it zeroes only the missing ones (on the call's
-// stream). With an unchanged problem shape nothing is written.
-std::mutex g_zero_mu;
-std::unordered_map<uintptr_t, int64_t> g_zero_counters;
+// ---- fused merge epochs ---------------------------------------------------------------
+// Every call gets a number no earlier call in the process had (never 0); its contributors
+// publish their partial states by writing it into their slots' flags. A zeroed workspace
+// holds no valid number, and flags left by earlier calls (completed, aborted, or through
+// another pointer into the same buffer) hold older ones, so no flag ever needs resetting.
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch() {
+  uint32_t e = ++g_epoch;
+  while (e == 0) e = ++g_epoch;
+  return e;
+}
 
 }  // namespace
 
-namespace pa {
-void forget_zeroed_workspaces() {
-  std::lock_guard<std::mutex> lk(g_zero_mu);
-  g_zero_counters.clear();
-}
-}  // namespace pa
-
 namespace {
-
-void note_zeroed(const void *ws, size_t bytes) {
-  std::lock_guard<std::mutex> lk(g_zero_mu);
-  g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = static_cast<int64_t>(bytes / 4);
-}
-
-// `fused`: this call merges through the counters, so the first `units` must be zero.
-// Either way the call writes partial states past its own counter region, so afterwards at
-// most `units` leading counters are known to be zero.
-pa_status_t prepare_counters(void *ws, int64_t units, bool fused, cudaStream_t stream) {
-  std::lock_guard<std::mutex> lk(g_zero_mu);
-  auto it = g_zero_counters.find(reinterpret_cast<uintptr_t>(ws));
-  int64_t known = it == g_zero_counters.end() ? 0 : it->second;
-  if (fused && units > known) {
-    if (cudaMemsetAsync(static_cast<char *>(ws) + known * 4, 0,
-                        static_cast<size_t>(units - known) * 4, stream) != cudaSuccess)
-      return PA_ERR_CUDA;
-    known = units;
-  }
-  g_zero_counters[reinterpret_cast<uintptr_t>(ws)] = std::min(known, units);
-  return PA_OK;
-}
 
 // ---- library-owned workspace ----------------------------------------------------------
 struct Workspace {
@@ -380,7 +355,6 @@ pa_status_t library_workspace(int dev, size_t need, cudaStream_t stream, void **
     }
     if (cudaMemsetAsync(w.ptr, 0, grow, stream) != cudaSuccess) return PA_ERR_CUDA;
     w.bytes = grow;
-    note_zeroed(w.ptr, grow);
   }
   *ptr = w.ptr;
   return PA_OK;
@@ -474,22 +448,13 @@ pa_status_t decode_into(const pa_problem_t *p, const void *q, const void *k, con
     const int64_t slots = units + pl.workers;
     auto al = [](int64_t x) { return (x + 255) / 256 * 256; };
     char *base = static_cast<char *>(ws);
-    a.ws_count = reinterpret_cast<int *>(base);
-    base += al(units * 4);
+    a.ws_flag = reinterpret_cast<unsigned *>(base);
+    base += al(slots * 4);
     a.ws_ml = reinterpret_cast<float *>(base);
     base += al(slots * kMaxHeads * 2 * 4);
     a.ws_acc = reinterpret_cast<float *>(base);
   }
-  if (a.mode == MODE_BALANCED) {
-    if (kind == WorkspaceKind::kZeroEachCall) {
-      if (a.fused &&
-          cudaMemsetAsync(ws, 0, static_cast<size_t>(pl.units) * 4, stream) != cudaSuccess)
-        return PA_ERR_CUDA;
-    } else {
-      st = prepare_counters(ws, pl.units, a.fused != 0, stream);
-      if (st != PA_OK) return st;
-    }
-  }
+  a.epoch = next_epoch();
   if (launch_decode(a, &tk, &tv, r.mma, r.nh_inst, r.plan.tile_tokens, pl.ctas, pl.warps_per_cta,
                     static_cast<size_t>(pl.smem_bytes), stream) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -538,7 +503,6 @@ pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *str
   if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return PA_ERR_CUDA;
-  note_zeroed(workspace, workspace_bytes);
   return PA_OK;
 }
 

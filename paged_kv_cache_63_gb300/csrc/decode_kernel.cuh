@@ -573,61 +573,115 @@ __device__ __forceinline__ void mma_tile(MmaState<HD> &st, const MmaLane<HD, T> 
 }
 
 // ------------------------------------------------------------------ merge (log-sum-exp)
+// Fused merge flags: a contributor publishes its partial state with a release store of the
+// call's epoch; the merger's acquire loads of every other contributor's flag then see the
+// states. Each call has its own epoch, so flags from earlier calls never match.
+__device__ __forceinline__ void flag_release(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned flag_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The merger of `unit` (contributor c0) waits until contributors c0 + 1 .. c0 + n - 1 have
+// published their states. Every lane polls every flag itself (the same addresses, one
+// transaction each), so each lane's later loads are ordered after its own acquire. Bounded:
+// after kWaitLimitNs it raises PA_DEVERR_TIMEOUT and returns false (the unit's rows are
+// then not written).
+__device__ __forceinline__ bool merge_wait(const KernelArgs &a, long long unit, long long c0,
+                                           int n) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    bool all = true;
+    for (int k = 1; k < n && all; ++k)
+      all = flag_acquire(a.ws_flag + slot_of(unit, c0 + k, a.group)) == a.epoch;
+    if (__all_sync(0xffffffffu, all)) return true;
+    __nanosleep(64);
+    if ((it & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) {
+      if ((threadIdx.x & 31) == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Merge the n partial states of one unit (balanced layout: slots unit + c0 .. unit + c0 +
-// n - 1) into normalised rows of `out`, all heads at once, by one warp. Two passes instead
-// of the sequential online merge, so that loads do not wait on each other: the common
-// maximum M_h per head first, then out_h = sum_k 2^(m_hk - M_h) acc_hk / sum_k 2^(m_hk - M_h)
-// l_hk, summed in contributor order (states with l = 0 are empty and skipped). Lanes own
-// head_dim / 32 dims.
+// n - 1) into normalised rows of `out`, all heads at once, by one warp: out_h = sum_k
+// 2^(m_hk - M_h) acc_hk / sum_k 2^(m_hk - M_h) l_hk with M_h the largest m_hk (states with
+// l = 0 are empty and skipped). Contributors are taken KB at a time, and for each batch the
+// (m, l) pairs (one per lane: lane = head * KB + contributor) and the accumulator rows
+// (lanes own head_dim / 32 dims) are loaded together, so a batch costs one memory round
+// trip; the running maximum, sum and rows are rescaled when a later batch raises the
+// maximum. Contributors are added in their order, so the result is deterministic.
 template <int HD>
 __device__ __forceinline__ void merge_balanced(const KernelArgs &a, long long unit, long long c0,
                                                int n, int b, int h0, int nh) {
   constexpr int DPL = HD / 32;
+  constexpr int KB = HD >= 256 ? 1 : 2;             // contributors per batch (registers)
+  constexpr int HG = HD >= 256 ? 4 : kMaxHeads;     // heads per pass (registers)
   const int lane = threadIdx.x & 31;
-  const int hl = lane >> 2;  // pass 1: lane (hl, lane & 3) scans contributors k = lane & 3 (mod 4)
-  float mx = -INFINITY;
-  if (hl < nh) {
-    for (int k = lane & 3; k < n; k += 4) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-          a.ws_ml + (slot_of(unit, c0 + k, a.group) * kMaxHeads + hl) * 2));
-      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-    }
-  }
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  float M[kMaxHeads];
-#pragma unroll
-  for (int h = 0; h < kMaxHeads; ++h) M[h] = __shfl_sync(0xffffffffu, mx, 4 * h);
-
-  // heads in groups of HG so the accumulators stay in registers
-  constexpr int HG = HD >= 256 ? 4 : kMaxHeads;
 #pragma unroll
   for (int g0 = 0; g0 < kMaxHeads; g0 += HG) {
     if (g0 >= nh) break;
-    float O[HG][DPL];
-    float L[HG];
+    float O[HG][DPL], L[HG], M[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
       L[h] = 0.f;
+      M[h] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < DPL; ++i) O[h][i] = 0.f;
     }
-#pragma unroll(HD >= 256 ? 1 : 2)
-    for (int k = 0; k < n; ++k) {
-      const long long slot = slot_of(unit, c0 + k, a.group);
-      const float *ml = a.ws_ml + (slot * kMaxHeads + g0) * 2;
-      const float *acc = a.ws_acc + (slot * kMaxHeads + g0) * HD + lane * DPL;
+    for (int k0 = 0; k0 < n; k0 += KB) {
+      // loads of the batch: lane (h, k) its (m, l); every lane its dims of every row
+      const int lk = lane % KB, lh = lane / KB;
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lh < HG && g0 + lh < nh && k0 + lk < n)
+        ml = __ldcg(reinterpret_cast<const float2 *>(
+            a.ws_ml + (slot_of(unit, c0 + k0 + lk, a.group) * kMaxHeads + g0 + lh) * 2));
+      float2 v[KB][HG][DPL / 2];
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        const bool kin = k0 + k < n;
+        const float *acc =
+            a.ws_acc + (slot_of(unit, c0 + (kin ? k0 + k : 0), a.group) * kMaxHeads + g0) * HD +
+            lane * DPL;
+#pragma unroll
+        for (int h = 0; h < HG; ++h)
+#pragma unroll
+          for (int i = 0; i < DPL / 2; ++i)
+            v[k][h][i] = (kin && g0 + h < nh)
+                             ? __ldcg(reinterpret_cast<const float2 *>(acc + h * HD + 2 * i))
+                             : make_float2(0.f, 0.f);
+      }
 #pragma unroll
       for (int h = 0; h < HG; ++h) {
-        if (g0 + h < nh) {
-          const float2 s = __ldcg(reinterpret_cast<const float2 *>(ml + 2 * h));
-          const float w = s.y > 0.f ? fast_exp2(s.x - M[g0 + h]) : 0.f;
-          L[h] += w * s.y;
+        // the batch's (m, l) of head h, from lanes h * KB .. h * KB + KB - 1
+        float mk[KB], lk2[KB];
+        float bm = -INFINITY;
 #pragma unroll
-          for (int i = 0; i < DPL; i += 2) {
-            const float2 v = __ldcg(reinterpret_cast<const float2 *>(acc + h * HD + i));
-            O[h][i] += w * v.x;
-            O[h][i + 1] += w * v.y;
+        for (int k = 0; k < KB; ++k) {
+          mk[k] = __shfl_sync(0xffffffffu, ml.x, (h * KB + k) & 31);
+          lk2[k] = __shfl_sync(0xffffffffu, ml.y, (h * KB + k) & 31);
+          if (lk2[k] > 0.f) bm = fmaxf(bm, mk[k]);
+        }
+        if (g0 + h >= nh || bm == -INFINITY) continue;  // warp-uniform
+        if (bm > M[h]) {
+          const float f = M[h] == -INFINITY ? 0.f : fast_exp2(M[h] - bm);
+          L[h] *= f;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) O[h][i] *= f;
+          M[h] = bm;
+        }
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+          const float w = lk2[k] > 0.f ? fast_exp2(mk[k] - M[h]) : 0.f;
+          L[h] += w * lk2[k];
+#pragma unroll
+          for (int i = 0; i < DPL / 2; ++i) {
+            O[h][2 * i] += w * v[k][h][i].x;
+            O[h][2 * i + 1] += w * v[k][h][i].y;
           }
         }
       }
@@ -924,16 +978,16 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     Ep::partial_out(st, cur, a.ws_ml + slot * kMaxHeads * 2, a.ws_ml + slot * kMaxHeads * 2 + 1,
                     a.ws_acc + slot * kMaxHeads * HD, 2, HD);
     if (!a.fused) return;
-    __threadfence();
     __syncwarp();
-    int old = 0;
-    if (lane == 0) old = atomicAdd(a.ws_count + unit, 1);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == n - 1) {
-      __threadfence();
-      merge_balanced<HD>(a, unit, c0, n, cur.b, cur.h0, cur.nh);
-      if (lane == 0) atomicExch(a.ws_count + unit, 0);
+    if (worker != c0) {
+      // The unit's merger is the worker holding its first tiles: it reaches them at the end
+      // of its range, after the others have written their states (at the start of their
+      // ranges, or over the whole of them). The flag's release store orders this warp's
+      // state writes before it; nothing else waits here.
+      if (lane == 0) flag_release(a.ws_flag + slot, a.epoch);
+      return;
     }
+    if (merge_wait(a, unit, c0, n)) merge_balanced<HD>(a, unit, c0, n, cur.b, cur.h0, cur.nh);
   };
 
   // ---- main loop: refill the slot freed last iteration, wait for the next tile, compute
@@ -981,28 +1035,9 @@ __global__ void __launch_bounds__(kMaxWarpsPerCta * 32, 1)
     // let the copies still in flight land before the shared memory is given up
     for (int i = consumed; i < issued; ++i)
       mbar_wait(bar0 + 8 * (i % S), static_cast<uint32_t>((i / S) & 1), a.err);
-    // Fused merge: still count this warp's arrival at the unit in hand and at every later
-    // unit of its range that it shares with other workers, so that each counter reaches its
-    // contributor count and its last arrival resets it to zero. The rows of those units
-    // are invalid (the error word says so), but the next call finds every counter at zero.
-    if (a.mode == MODE_BALANCED && a.fused) {
-      for (;;) {
-        const long long unit = static_cast<long long>(cur.b) * a.ups + cur.us;
-        const int nt = tiles_of(cur_end, T);
-        const long long c0 = worker_of(cur_ug0, total, nworkers);
-        const long long c1 = worker_of(cur_ug0 + nt - 1, total, nworkers);
-        if (c1 > c0 && lane == 0) {
-          if (atomicAdd(a.ws_count + unit, 1) == static_cast<int>(c1 - c0))
-            atomicExch(a.ws_count + unit, 0);
-        }
-        c.left -= nt - c.tok / T;  // the unit's tiles from the current one on
-        if (c.left <= 0) break;
-        next_unit(a, c, T);
-        cur = unit_info(a, c.b, c.us * a.group + member);
-        cur_ug0 = c.ug0;
-        cur_end = c.end;
-      }
-    }
+    // Fused merge: this warp's flags stay unset, so a merger waiting on them gives up
+    // (bounded) and the call reports the timeout; the next call's epoch differs from every
+    // flag written so far, so nothing needs resetting.
     return;
   }
   finish_unit();

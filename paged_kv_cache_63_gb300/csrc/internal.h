@@ -34,7 +34,8 @@ struct KernelArgs {
   // balanced-schedule workspace
   float *ws_ml;   // [slots][kMaxHeads][2]  (max in base-2 units, sum)
   float *ws_acc;  // [slots][kMaxHeads][head_dim]
-  int *ws_count;  // [units]  merge counters, zero between calls
+  unsigned *ws_flag;  // [slots] fused merge: holds the call's epoch once the slot's partial
+                      // state is written
   // fixed-split partial arrays: [batch][splits][query_heads]([head_dim])
   float *p_max;
   float *p_sum;
@@ -53,7 +54,9 @@ struct KernelArgs {
   int mode;
   int num_splits;  // MODE_SPLIT
   int workers;     // MODE_BALANCED: number of workers (groups of `group` warps)
-  int fused;       // MODE_BALANCED: last worker merges
+  int fused;       // MODE_BALANCED: each shared unit is merged by the worker holding its
+                   // first tiles, once the other contributors' flags show `epoch`
+  unsigned epoch;  // this call's number (never 0), unique within the process
   int stages;
   int warp_smem;   // bytes of dynamic shared memory per warp (multiple of kSmemAlign)
   unsigned tx_extra;  // bytes the first tile of each warp waits for beyond what it loads
@@ -117,10 +120,6 @@ cudaError_t launch_combine_balanced(const KernelArgs &a, int units, int heads, i
 cudaError_t launch_combine_split(const KernelArgs &a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags);
 unsigned *device_error_word();
-// Drop every record of workspace merge counters known to be zero (api.cpp), so that the
-// next call on each workspace zeroes its counters again; called when the error word shows
-// an expired wait.
-void forget_zeroed_workspaces();
 
 }  // namespace pa
 
@@ -128,11 +127,11 @@ void forget_zeroed_workspaces();
 
 namespace pa {
 
-// Who owns a decode call's workspace and how its merge counters are brought to zero.
+// Who owns a decode call's workspace.
 enum class WorkspaceKind {
-  kLibrary,      // library-owned grow-only buffer (pa_decode)
-  kCaller,       // caller buffer zeroed once by pa_workspace_init (pa_decode_ex)
-  kZeroEachCall  // fixed buffer whose counters are cleared on the stream before every call
+  kLibrary,  // library-owned grow-only buffer, zeroed when allocated (pa_decode)
+  kCaller,   // caller buffer zeroed once by pa_workspace_init (pa_decode_ex)
+  kStatic    // the library's fixed scratch array, zero at load (pa_decode_noalloc)
 };
 
 // Host-side argument checks shared by the entry points (no GPU access).

@@ -104,10 +104,6 @@ cudaError_t read_and_clear_device_error(cudaStream_t stream, uint32_t *flags) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof(unsigned), stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-  // an expired wait may have left merge counters mid-count in whichever workspace that call
-  // used; the kernels count the missing arrivals themselves, and this makes the next call on
-  // any workspace zero its counters as well
-  if (v & PA_DEVERR_TIMEOUT) forget_zeroed_workspaces();
   *flags = v;
   return e;
 }

@@ -55,10 +55,10 @@ extern "C" pa_status_t pa_decode_noalloc(const pa_problem_t *problem, const void
   void *scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != PA_OK) return st;
-  // The merge counters at the start of the scratch are cleared on `stream` before each
-  // call; a plan needing more than PA_NOALLOC_SCRATCH_BYTES is refused with
-  // PA_ERR_WORKSPACE before anything is launched.
+  // The fused merge's flags in the scratch need no clearing (each call publishes states
+  // under its own number); a plan needing more than PA_NOALLOC_SCRATCH_BYTES is refused
+  // with PA_ERR_WORKSPACE before anything is launched.
   return pa::decode_into(problem, query, key_cache, value_cache, block_tables, context_lengths,
                          scale, out, nullptr, scratch, PA_NOALLOC_SCRATCH_BYTES,
-                         pa::WorkspaceKind::kZeroEachCall, static_cast<cudaStream_t>(stream));
+                         pa::WorkspaceKind::kStatic, static_cast<cudaStream_t>(stream));
 }

@@ -116,7 +116,7 @@ def test_workspace_errors_and_reuse():
     assert lib.status_of(lib.pa_decode_ex, *args, ws.data_ptr() + 16, n) == 3
     lib.pa_workspace_init(ws, n)
     outs = []
-    for _ in range(3):  # the merge counters return to zero after every call
+    for _ in range(3):  # reused as it is: nothing in it needs resetting between calls
         lib.pa_decode_ex(*args, ws, n)
         t.cuda.synchronize()
         outs.append(d["out"].cpu().numpy().copy())
@@ -143,7 +143,9 @@ def test_side_stream():
 def test_workspace_follows_shape_changes():
     """One workspace (library-owned, and one caller buffer) across problems whose unit
     counts grow and shrink, with the caller buffer's calls alternating between the fused
-    merge and the combine kernel: merge counters must start at zero every time."""
+    merge and the combine kernel and between two start addresses 256 bytes apart (so each
+    call's flags lie over states and flags that other calls wrote): a flag left by an
+    earlier call must never pass for one of this call's."""
     import oracle
 
     t = torch()
@@ -156,12 +158,12 @@ def test_workspace_follows_shape_changes():
         assert_close(run(w), ref, f"pa_decode {w.name} b={w.batch}")
     combos = [lib.options(schedule="balanced", combine=c) for c in ("fused", "kernel")]
     n = max(lib.pa_workspace_size(lib.problem_of(w), o) for w in seq for o in combos)
-    ws = t.empty(n, dtype=t.uint8, device="cuda")
-    lib.pa_workspace_init(ws, n)
+    ws = t.empty(n + 256, dtype=t.uint8, device="cuda")
+    lib.pa_workspace_init(ws, n + 256)
     for i, (w, ref) in enumerate(zip(seq, refs)):
         d = to_device(w)
         lib.pa_decode_ex(lib.problem_of(w), d["q"], d["k"], d["v"], d["bt"], d["ctx"], w.scale,
-                         d["out"], combos[i % 2], ws, n)
+                         d["out"], combos[i % 2], ws.data_ptr() + 256 * ((i // 2) % 2), n)
         t.cuda.synchronize()
         assert_close(d["out"].cpu().numpy(), ref, f"pa_decode_ex {w.name} b={w.batch}")
 
@@ -194,12 +196,13 @@ def test_expired_wait_is_reported_and_device_stays_usable():
 
 
 @pytest.mark.parametrize("case", ["forced_96_workers", "default_plan"])
-def test_expired_wait_leaves_fused_merge_counters_at_zero(case):
-    """With more units than workers the last worker of each shared unit merges it, counted
-    by a per-unit counter in the workspace. Warps whose waits expire must still count their
-    arrivals, so the counters are back at zero when the call ends, and the next call on the
-    same workspace -- without pa_workspace_init and before the error word is read -- is
-    correct; the one after reading the error word too."""
+def test_expired_wait_in_fused_merge_then_correct_calls(case):
+    """With more units than workers each shared unit is merged inside the decode kernel by
+    the worker holding its first tiles, once the others have published their states (a flag
+    per state holding the call's number). Under PA_TEST_EXPIRE_WAITS every warp gives up on
+    its first tile, so no state is published and no merge runs; the next call on the same
+    workspace -- without pa_workspace_init and before the error word is read -- is correct,
+    and so is the one after reading the error word."""
     import oracle
 
     t = torch()
@@ -224,8 +227,6 @@ def test_expired_wait_leaves_fused_merge_counters_at_zero(case):
     assert_close(d["out"].cpu().numpy(), ref, "before")
     lib.pa_decode_ex(*args, bad, ws, n)
     t.cuda.synchronize()
-    counters = ws[:pl["units"] * 4].view(t.int32).cpu().numpy()
-    assert not counters.any(), f"{int((counters != 0).sum())} merge counters left nonzero"
     d["out"].fill_(float("nan"))
     lib.pa_decode_ex(*args, good, ws, n)
     t.cuda.synchronize()

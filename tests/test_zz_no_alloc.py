@@ -17,7 +17,7 @@ from tests.gpu_util import assert_close, to_device, torch
 pytestmark = pytest.mark.gpu
 
 # (workload, overrides, merge the default plan picks: 1 = fused in the decode kernel, 2 =
-# separate combine kernel). The fused merge is the path whose counters live in the scratch.
+# separate combine kernel). The fused merge is the path whose flags live in the scratch.
 WORKLOADS = {
     "gqa4_mid": ("gqa4_mid", dict(), 2),
     "ragged_b64": ("ragged", dict(batch=64), 2),
