@@ -105,15 +105,6 @@ __device__ __forceinline__ bool clc_query(uint32_t answer, int &x, int &y, int &
   return ok != 0;
 }
 
-// 32-byte store (one full sector) of 8 floats with an L2 eviction-priority policy.
-__device__ __forceinline__ void st_global_v8(float *p, float v0, float v1, float v2, float v3,
-                                             float v4, float v5, float v6, float v7, uint64_t pol) {
-  asm volatile(
-      "st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
-      "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7), "l"(pol)
-      : "memory");
-}
-
 // Geometry of one work item (K/V head kv, sequence b, pair of query tiles), computed once by
 // the scheduler and published to every role. `live` is 0 when the pair holds no new token
 // or the sequence's offsets or length are out of range (those are flagged here); `stop` marks

@@ -108,6 +108,15 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// 32-byte store (one full sector) of 8 floats with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_global_v8(float *p, float v0, float v1, float v2, float v3,
+                                             float v4, float v5, float v6, float v7, uint64_t pol) {
+  asm volatile(
+      "st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+      "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -381,27 +390,30 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
       }
-      // scaled scores (log2 units); keys past this row's position are masked out
+      // keys past this row's position are masked out; the row maximum of the scaled scores
+      // (log2 units) is the extreme raw score times the scale (the maximum for a
+      // non-negative scale, else the minimum), which saves a multiply per score; eight
+      // independent partial extremes keep the reduction off one dependency chain
       const int lim = pos - j * C::TN;
-      // eight independent partial maxima and sums keep the reductions off one dependency chain
+      const bool full = lim >= C::TN - 1;
       float mp[8];
+      float ext;
+      if (sl2 >= 0.f) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-      if (lim >= C::TN - 1) {
+        for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < C::TN; ++c) {
-          x[c] *= sl2;
-          mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-        }
+        for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], (full || c <= lim) ? x[c] : -INFINITY);
+        ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       } else {
 #pragma unroll
-        for (int c = 0; c < C::TN; ++c) {
-          x[c] = c <= lim ? x[c] * sl2 : -INFINITY;
-          mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-        }
+        for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
+#pragma unroll
+        for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? x[c] : INFINITY);
+        ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
+                    fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const float mx = ext * sl2;
       const bool grow = mx > m + kPrefillRescaleSlack;
       if (__any_sync(0xffffffffu, grow)) {
         const float mnew = grow ? mx : m;
@@ -425,13 +437,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         m = mnew;
       }
+      // P = exp2(s * scale * log2e - m): the scale is folded into one FMA per score (packed
+      // fp32 pairs: one FFMA2 for two exponents, one FADD2 for two sums); masked keys give 0
       float rp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) rp[e] = 0.f;
+      const float nm = -m;
 #pragma unroll
-      for (int c = 0; c < C::TN; ++c) {
-        x[c] = prefill_exp2(x[c] - m);
-        rp[c & 7] += x[c];
+      for (int c = 0; c < C::TN; c += 2) {
+        const float2 xx =
+            ffma2(make_float2(x[c], x[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+        const float p0 = (full || c <= lim) ? prefill_exp2(xx.x) : 0.f;
+        const float p1 = (full || c + 1 <= lim) ? prefill_exp2(xx.y) : 0.f;
+        const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
+        rp[c & 7] = acc.x;
+        rp[(c + 1) & 7] = acc.y;
+        x[c] = p0;
+        x[c + 1] = p1;
       }
       l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
       // P buffer st was last read by the P.V of tile j - 2
@@ -461,15 +483,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float *dst = a.out + (static_cast<size_t>(q0 + tok0 + t) * a.qh + kv * a.g + h) * HD;
+      // whole 32-byte sectors where out allows (L2 then never fills a partly written sector
+      // from DRAM); the output is read by no kernel here, so it leaves L2 first
+      const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) {
         float v[32];
         tmem_ld32(trow + C::kOCol + c * 32, v);
-        if (valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4 *>(dst + c * 32 + e) =
-                make_float4(v[e] * inv, v[e + 1] * inv, v[e + 2] * inv, v[e + 3] * inv);
+        for (int e = 0; e < 32; ++e) v[e] *= inv;
+        if (valid) {
+          if (a.out_v8) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+              st_global_v8(dst + c * 32 + e, v[e], v[e + 1], v[e + 2], v[e + 3], v[e + 4],
+                           v[e + 5], v[e + 6], v[e + 7], pol);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4 *>(dst + c * 32 + e) =
+                  make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          }
         }
       }
     }
