@@ -76,35 +76,6 @@ enum : int {
   kNumBars2 = 31
 };
 
-// ---- cluster launch control -------------------------------------------------------------
-// Ask for one CTA of this grid that has not started to be cancelled so that the caller runs
-// its work; the 16-byte answer is written to shared memory and completes `bar` with 16 bytes
-// of transaction count.
-__device__ __forceinline__ void clc_try_cancel(uint32_t answer, uint32_t bar) {
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
-      " [%0], [%1];" ::"r"(answer), "r"(bar)
-      : "memory");
-}
-
-// Read an answer: true and the cancelled CTA's index if a CTA was cancelled, false when
-// every CTA of the grid has started (no work is left to take).
-__device__ __forceinline__ bool clc_query(uint32_t answer, int &x, int &y, int &z) {
-  uint32_t ok, cx = 0, cy = 0, cz = 0;
-  asm volatile(
-      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\tld.shared.b128 r, [%4];\n\t"
-      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
-      "selp.u32 %3, 1, 0, p;\n\t"
-      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, %1, %2, _}, r;\n\t}"
-      : "+r"(cx), "+r"(cy), "+r"(cz), "=r"(ok)
-      : "r"(answer)
-      : "memory");
-  x = static_cast<int>(cx);
-  y = static_cast<int>(cy);
-  z = static_cast<int>(cz);
-  return ok != 0;
-}
-
 // Geometry of one work item (K/V head kv, sequence b, pair of query tiles), computed once by
 // the scheduler and published to every role. `live` is 0 when the pair holds no new token
 // or the sequence's offsets or length are out of range (those are flagged here); `stop` marks
