@@ -458,20 +458,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           ok = pipe_wait(bar(kBarKFull + st), (t >> 1) & 1, abort_flag, a.err);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
+          {
+            // issued warp-collectively by one elected lane of the converged warp, with
+            // descriptors = base descriptor + step offset / 16 (the empty asm keeps the
+            // compiler from hoisting every step's descriptor into registers)
             const uint32_t d = tmem + st * C::TN;
+            uint64_t qd = smem_desc_sw128(sq, 16, 1024);
+            uint64_t kd = smem_desc_sw128(k_stage(st), 16, 1024);
+            asm volatile("" : "+l"(qd), "+l"(kd));
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * (C::TN * 128) + (ks & 3) * 32;
-              const uint64_t ad = smem_desc_sw128(sq + (ks >> 2) * (C::kRows * 128) + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(k_stage(st) + off, 16, 1024);
-              mma_f16_ss(d, ad, bd, C::kIdescS, ks > 0);
+              const uint64_t ad = qd + (((ks >> 2) * (C::kRows * 128) + (ks & 3) * 32) >> 4);
+              const uint64_t bd = kd + (((ks >> 2) * (C::TN * 128) + (ks & 3) * 32) >> 4);
+              mma_f16_ss_warp(d, ad, bd, C::kIdescS, ks > 0);
             }
-            mma_commit(bar(kBarSFull + st));
-            mma_commit(bar(kBarKEmpty + st));
-            if (j == it.ntiles - 1) mma_commit(bar(kBarQEmpty));
+            mma_commit_warp(bar(kBarSFull + st));
+            mma_commit_warp(bar(kBarKEmpty + st));
+            if (j == it.ntiles - 1) mma_commit_warp(bar(kBarQEmpty));
           }
-          __syncwarp();
         }
         if (j >= 1) {
           const int i = j - 1, t = g + i, st = t & 1;
@@ -492,28 +496,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             fence_proxy_async();
             __syncwarp();
           }
-          if (lane == 0) {
+          {
             // the item's first P.V overwrites O: the softmax released this P only after it
             // had read the previous item's O
+            uint64_t pd = smem_desc_sw128(p_buf(st), 16, 1024);
+            uint64_t vd = smem_desc_sw128(v_stage(st), C::TN * 128, 1024);
+            asm volatile("" : "+l"(pd), "+l"(vd));
 #pragma unroll
             for (int ks = 0; ks < C::TN / 16; ++ks) {
-              const uint64_t ad = smem_desc_sw128(p_buf(st) + (ks >> 2) * (C::kRows * 128) + (ks & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(v_stage(st) + ks * 2048, C::TN * 128, 1024);
-              mma_f16_ss(tmem + C::kOCol, ad, bd, C::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+              const uint64_t ad = pd + (((ks >> 2) * (C::kRows * 128) + (ks & 3) * 32) >> 4);
+              const uint64_t bd = vd + ((ks * 2048) >> 4);
+              mma_f16_ss_warp(tmem + C::kOCol, ad, bd, C::kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
             }
-            mma_commit(bar(kBarPV + st));
-            mma_commit(bar(kBarVEmpty + st));
+            mma_commit_warp(bar(kBarPV + st));
+            mma_commit_warp(bar(kBarVEmpty + st));
           }
-          __syncwarp();
         }
       }
       g += it.ntiles;
     }
-    // every MMA this thread issued has completed before TMEM is released
-    if (lane == 0) {
-      mma_commit(bar(kBarDone));
-      drain_wait(bar(kBarDone), 0, a.err);
-    }
+    // every MMA this warp issued has completed before TMEM is released
+    mma_commit_warp(bar(kBarDone));
+    if (lane == 0) drain_wait(bar(kBarDone), 0, a.err);
     __syncwarp();
   } else if (warp >= 2 && warp <= 5) {
     // ================= softmax: one query row per thread =================
