@@ -121,6 +121,33 @@ __device__ __forceinline__ Item2 item2_of(const PrefillArgs &a, int kv, int b, i
   return it;
 }
 
+// P = exp2(s * sl2 + nm) over a full row of TN scores (no key masked), written as fp16 pairs
+// over the first TN / 2 TMEM columns at ts, with the row's partial sums in rp. Packed fp32
+// pairs: one FFMA2 gives two exponent arguments and one FADD2 adds two terms to the sums.
+template <int TN>
+__device__ __forceinline__ void exps_full(const float (&v)[TN], float sl2, float nm, uint32_t ts,
+                                          float (&rp)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rp[e] = 0.f;
+#pragma unroll
+  for (int h2 = 0; h2 < TN / 64; ++h2) {
+    float pk[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = h2 * 64 + 2 * e;
+      const float2 xx =
+          ffma2(make_float2(v[c], v[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+      const float p0 = prefill_exp2(xx.x);
+      const float p1 = prefill_exp2(xx.y);
+      const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
+      rp[c & 7] = acc.x;
+      rp[(c + 1) & 7] = acc.y;
+      pk[e] = __uint_as_float(pack_half2(p0, p1));
+    }
+    tmem_st32(ts + h2 * 32, pk);
+  }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kPrefill2Threads, 1)
     prefill2_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ CUtensorMap tq,
@@ -492,93 +519,91 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
             ok = pipe_wait(bar(kB2Full + ik % C::kSlots), (ik / C::kSlots) & 1, abort_flag, a.err);
           if (!ok) break;
         }
-        // keys past this row's position are masked out (on tiles that reach the diagonal);
-        // the row maximum of the scaled scores is the extreme raw score times the scale (the
-        // maximum for a non-negative scale, else the minimum), which saves a multiply per score
         const int lim = pos - j * C::TN;
-        float mp[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-        // warp-uniform: the exponent pass below holds tcgen05.st, which the whole warp executes
+        // warp-uniform: the exponent passes hold tcgen05.st, which the whole warp executes
         const bool full = __all_sync(0xffffffffu, lim >= C::TN - 1);
-        float ext;
-        if (sl2 >= 0.f) {
-          if (full) {
+        float rp[8];
+        // After a row's first tile its running maximum m seldom grows by more than the slack,
+        // so a full tile first takes its exponents with m as it stands and no maximum pass:
+        // the terms are non-negative, so the tile's row sum bounds each of them, and a sum of
+        // at most 2^slack shows that no score passed m + slack. Only a warp in which some row's
+        // sum is larger (or not a number) takes the tile again in the plain order: maximum,
+        // rescale, exponents.
+        bool redo = true;
+        if (full && j > 0) {
+          exps_full<C::TN>(v, sl2, -m, ts, rp);
+          const float tsum =
+              ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+          redo = __any_sync(0xffffffffu, !(tsum <= kPrefillSlackBound));
+          if (redo) tmem_wait_st();  // the plain pass below rewrites the same columns
+        }
+        if (redo) {
+          // keys past this row's position are masked out (on tiles that reach the diagonal);
+          // the row maximum of the scaled scores is the extreme raw score times the scale (the
+          // maximum for a non-negative scale, else the minimum), which saves a multiply per score
+          float mp[8];
 #pragma unroll
-            for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], v[c]);
+          for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
+          float ext;
+          if (sl2 >= 0.f) {
+            if (full) {
+#pragma unroll
+              for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], v[c]);
+            } else {
+#pragma unroll
+              for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], c <= lim ? v[c] : -INFINITY);
+            }
+            ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                        fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
           } else {
 #pragma unroll
-            for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], c <= lim ? v[c] : -INFINITY);
+            for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? v[c] : INFINITY);
+            ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
+                        fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
           }
-          ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        } else {
+          const float mx = ext * sl2;
+          const bool grow = mx > m + kPrefillRescaleSlack;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float mnew = grow ? mx : m;
+            const float f = mnew == -INFINITY ? 1.f : prefill_exp2(m - mnew);
+            l *= f;
+            if (j > 0) {
+              // S_X(j) completed, so PV_X(j - 1) has too: O_X is stable until P_X(j) is released
 #pragma unroll
-          for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
+              for (int c = 0; c < HD / 32; ++c) {
+                float o[32];
+                tmem_ld32(to + c * 32, o);
 #pragma unroll
-          for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? v[c] : INFINITY);
-          ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
-                      fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
-        }
-        const float mx = ext * sl2;
-        const bool grow = mx > m + kPrefillRescaleSlack;
-        if (__any_sync(0xffffffffu, grow)) {
-          const float mnew = grow ? mx : m;
-          const float f = mnew == -INFINITY ? 1.f : prefill_exp2(m - mnew);
-          l *= f;
-          if (j > 0) {
-            // S_X(j) completed, so PV_X(j - 1) has too: O_X is stable until P_X(j) is released
-#pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-              float o[32];
-              tmem_ld32(to + c * 32, o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= f;
-              tmem_st32(to + c * 32, o);
+                for (int e = 0; e < 32; ++e) o[e] *= f;
+                tmem_st32(to + c * 32, o);
+              }
             }
+            m = mnew;
           }
-          m = mnew;
-        }
-        // P = exp2(s * scale * log2e - m) as fp16 pairs over the first 64 columns of S (the
-        // scale is folded into one FFMA per score; masked keys give exactly 0)
-        float rp[8];
+          // P = exp2(s * scale * log2e - m) as fp16 pairs over the first 64 columns of S (the
+          // scale is folded into one FFMA per score; masked keys give exactly 0)
+          const float nm = -m;
+          if (full) {
+            exps_full<C::TN>(v, sl2, nm, ts, rp);
+          } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rp[e] = 0.f;
-        const float nm = -m;
-        if (full) {
+            for (int e = 0; e < 8; ++e) rp[e] = 0.f;
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            float pk[32];
+            for (int h2 = 0; h2 < 2; ++h2) {
+              float pk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = h2 * 64 + 2 * e;
-              // packed fp32 pairs: one FFMA2 for both exponents, one FADD2 for both sums
-              const float2 xx =
-                  ffma2(make_float2(v[c], v[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-              const float p0 = prefill_exp2(xx.x);
-              const float p1 = prefill_exp2(xx.y);
-              const float2 acc =
-                  fadd2(make_float2(rp[(2 * e) & 7], rp[(2 * e + 1) & 7]), make_float2(p0, p1));
-              rp[(2 * e) & 7] = acc.x;
-              rp[(2 * e + 1) & 7] = acc.y;
-              pk[e] = __uint_as_float(pack_half2(p0, p1));
+              for (int e = 0; e < 32; ++e) {
+                const int c = h2 * 64 + 2 * e;
+                const float p0 = c <= lim ? prefill_exp2(fmaf(v[c], sl2, nm)) : 0.f;
+                const float p1 = c + 1 <= lim ? prefill_exp2(fmaf(v[c + 1], sl2, nm)) : 0.f;
+                rp[(2 * e) & 7] += p0;
+                rp[(2 * e + 1) & 7] += p1;
+                pk[e] = __uint_as_float(pack_half2(p0, p1));
+              }
+              tmem_st32(ts + h2 * 32, pk);
             }
-            tmem_st32(ts + h2 * 32, pk);
-          }
-        } else {
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            float pk[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = h2 * 64 + 2 * e;
-              const float p0 = c <= lim ? prefill_exp2(fmaf(v[c], sl2, nm)) : 0.f;
-              const float p1 = c + 1 <= lim ? prefill_exp2(fmaf(v[c + 1], sl2, nm)) : 0.f;
-              rp[(2 * e) & 7] += p0;
-              rp[(2 * e + 1) & 7] += p1;
-              pk[e] = __uint_as_float(pack_half2(p0, p1));
-            }
-            tmem_st32(ts + h2 * 32, pk);
           }
         }
         l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));

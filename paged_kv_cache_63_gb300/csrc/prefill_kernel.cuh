@@ -70,6 +70,7 @@ constexpr int kPrefillSchedWarp = 7;
 // warps that read each published work item: 0, 1, the softmax warps 2..5 and 6
 constexpr int kItemReaders1 = 7;
 constexpr float kPrefillRescaleSlack = 8.f;  // log2 units: O is rescaled when m grows > 2^8
+constexpr float kPrefillSlackBound = 256.f;  // 2^kPrefillRescaleSlack
 
 // Barrier slots.
 enum : int {
