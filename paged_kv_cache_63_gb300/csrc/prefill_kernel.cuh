@@ -121,6 +121,27 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
+// P = exp2(s * sl2 + nm) over a row of TN scores, in place, with keys past lim (when the row
+// is not full) giving exactly 0, and the row's partial sums in rp. Packed fp32 pairs: one
+// FFMA2 gives two exponent arguments and one FADD2 adds two terms to the sums.
+template <int TN>
+__device__ __forceinline__ void exps_row(float (&x)[TN], float sl2, float nm, bool full, int lim,
+                                         float (&rp)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) rp[e] = 0.f;
+#pragma unroll
+  for (int c = 0; c < TN; c += 2) {
+    const float2 xx = ffma2(make_float2(x[c], x[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+    const float p0 = (full || c <= lim) ? prefill_exp2(xx.x) : 0.f;
+    const float p1 = (full || c + 1 <= lim) ? prefill_exp2(xx.y) : 0.f;
+    const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
+    rp[c & 7] = acc.x;
+    rp[(c + 1) & 7] = acc.y;
+    x[c] = p0;
+    x[c + 1] = p1;
+  }
+}
+
 // 32-byte store (one full sector) of 8 floats with an L2 eviction-priority policy.
 __device__ __forceinline__ void st_global_v8(float *p, float v0, float v1, float v2, float v3,
                                              float v4, float v5, float v6, float v7, uint64_t pol) {
@@ -550,70 +571,80 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
         }
-        // keys past this row's position are masked out; the row maximum of the scaled scores
-        // (log2 units) is the extreme raw score times the scale (the maximum for a
-        // non-negative scale, else the minimum), which saves a multiply per score; eight
-        // independent partial extremes keep the reduction off one dependency chain
         const int lim = pos - j * C::TN;
         const bool full = lim >= C::TN - 1;
-        float mp[8];
-        float ext;
-        if (sl2 >= 0.f) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], (full || c <= lim) ? x[c] : -INFINITY);
-          ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                      fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
-#pragma unroll
-          for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? x[c] : INFINITY);
-          ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
-                      fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
-        }
-        const float mx = ext * sl2;
-        const bool grow = mx > m + kPrefillRescaleSlack;
-        if (__any_sync(0xffffffffu, grow)) {
-          const float mnew = grow ? mx : m;
-          // 0 on the first tile (m = -inf); 1 for rows whose maximum did not grow
-          const float f = mnew == -INFINITY ? 1.f : prefill_exp2(m - mnew);
-          l *= f;
-          if (j > 0) {
-            // O holds tiles < j: wait for the last P.V, then scale this row of O in TMEM
-            ok = pipe_wait(bar(kBarPV + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1, abort_flag, a.err);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-              float v[32];
-              tmem_ld32(trow + C::kOCol + c * 32, v);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) v[e] *= f;
-              tmem_st32(trow + C::kOCol + c * 32, v);
-            }
-            tmem_wait_st();
-          }
-          m = mnew;
-        }
-        // P = exp2(s * scale * log2e - m): the scale is folded into one FMA per score (packed
-        // fp32 pairs: one FFMA2 for two exponents, one FADD2 for two sums); masked keys give 0
         float rp[8];
+        // After a row's first tile its running maximum m seldom grows by more than the slack,
+        // so when no row of the warp masks a key of this tile the exponents are first taken
+        // with m as it stands and no maximum pass: the terms are non-negative, so the tile's
+        // row sum bounds each of them, and a sum of at most 2^slack shows that no score passed
+        // m + slack. Only a warp in which some row's sum is larger (or not a number) reloads
+        // the scores and takes the plain order: maximum, rescale, exponents.
+        bool redo = true;
+        if (j > 0 && __all_sync(0xffffffffu, full)) {
+          exps_row<C::TN>(x, sl2, -m, true, lim, rp);
+          const float tsum =
+              ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
+          redo = __any_sync(0xffffffffu, !(tsum <= kPrefillSlackBound));
+          if (redo) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rp[e] = 0.f;
-        const float nm = -m;
+            for (int c = 0; c < C::TN / 32; ++c) {
+              float v[32];
+              tmem_ld32(trow + st * C::TN + c * 32, v);
 #pragma unroll
-        for (int c = 0; c < C::TN; c += 2) {
-          const float2 xx =
-              ffma2(make_float2(x[c], x[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-          const float p0 = (full || c <= lim) ? prefill_exp2(xx.x) : 0.f;
-          const float p1 = (full || c + 1 <= lim) ? prefill_exp2(xx.y) : 0.f;
-          const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
-          rp[c & 7] = acc.x;
-          rp[(c + 1) & 7] = acc.y;
-          x[c] = p0;
-          x[c + 1] = p1;
+              for (int e = 0; e < 32; ++e) x[c * 32 + e] = v[e];
+            }
+          }
+        }
+        if (redo) {
+          // keys past this row's position are masked out; the row maximum of the scaled scores
+          // (log2 units) is the extreme raw score times the scale (the maximum for a
+          // non-negative scale, else the minimum), which saves a multiply per score; eight
+          // independent partial extremes keep the reduction off one dependency chain
+          float mp[8];
+          float ext;
+          if (sl2 >= 0.f) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mp[e] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::TN; ++c) mp[c & 7] = fmaxf(mp[c & 7], (full || c <= lim) ? x[c] : -INFINITY);
+            ext = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                        fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mp[e] = INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::TN; ++c) mp[c & 7] = fminf(mp[c & 7], (full || c <= lim) ? x[c] : INFINITY);
+            ext = fminf(fminf(fminf(mp[0], mp[1]), fminf(mp[2], mp[3])),
+                        fminf(fminf(mp[4], mp[5]), fminf(mp[6], mp[7])));
+          }
+          const float mx = ext * sl2;
+          const bool grow = mx > m + kPrefillRescaleSlack;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float mnew = grow ? mx : m;
+            // 0 on the first tile (m = -inf); 1 for rows whose maximum did not grow
+            const float f = mnew == -INFINITY ? 1.f : prefill_exp2(m - mnew);
+            l *= f;
+            if (j > 0) {
+              // O holds tiles < j: wait for the last P.V, then scale this row of O in TMEM
+              ok = pipe_wait(bar(kBarPV + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1, abort_flag, a.err);
+              if (!ok) break;
+              tc_fence_after();
+#pragma unroll
+              for (int c = 0; c < HD / 32; ++c) {
+                float v[32];
+                tmem_ld32(trow + C::kOCol + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] *= f;
+                tmem_st32(trow + C::kOCol + c * 32, v);
+              }
+              tmem_wait_st();
+            }
+            m = mnew;
+          }
+          // P = exp2(s * scale * log2e - m): the scale is folded into one FMA per score (packed
+          // fp32 pairs: one FFMA2 for two exponents, one FADD2 for two sums); masked keys give 0
+          exps_row<C::TN>(x, sl2, -m, full, lim, rp);
         }
         l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
         // P buffer st was last read by the P.V of global tile gj - 2

@@ -98,11 +98,14 @@ def test_prefill_grid_taller_than_needed_and_untouched_rows():
     assert_close(got[:p.total], oracle.prefill(p.cache, p.query, p.query_start), "tall grid")
 
 
-def test_prefill_rescale_path():
+@pytest.mark.parametrize("head_dim", [128, 256])  # the two-tile and the single-tile kernel
+def test_prefill_rescale_path(head_dim):
     """Keys that grow along the sequence push each row's running maximum up by far more than
-    2^8 after the first key tile, so O is rescaled in TMEM many times."""
+    2^8 after the first key tile, so O is rescaled in TMEM many times, and full key tiles whose
+    exponents were first taken with the old maximum are taken again."""
+    extra = dict(query_heads=24, kv_heads=4, head_dim=256, page_size=64) if head_dim == 256 else {}
     p = make_prefill("prefill_chunked", context_lengths=[900, 520], new_tokens=[900, 300],
-                     max_pages_per_sequence=64)
+                     max_pages_per_sequence=64, **extra)
     w = p.cache
     k = w.key_cache.astype(np.float32)
     for b in range(w.batch):
