@@ -121,12 +121,13 @@ __device__ __forceinline__ Item2 item2_of(const PrefillArgs &a, int kv, int b, i
   return it;
 }
 
-// P = exp2(s * sl2 + nm) over a full row of TN scores (no key masked), written as fp16 pairs
-// over the first TN / 2 TMEM columns at ts, with the row's partial sums in rp. Packed fp32
-// pairs: one FFMA2 gives two exponent arguments and one FADD2 adds two terms to the sums.
-template <int TN>
-__device__ __forceinline__ void exps_full(const float (&v)[TN], float sl2, float nm, uint32_t ts,
-                                          float (&rp)[8]) {
+// P = exp2(s * sl2 + nm) over a row of TN scores, written as fp16 pairs over the first TN / 2
+// TMEM columns at ts, with the row's partial sums in rp. With kMasked keys past lim give
+// exactly 0; without, packed fp32 pairs do two exponent arguments per FFMA2 and two sum terms
+// per FADD2.
+template <int TN, bool kMasked>
+__device__ __forceinline__ void exps_row(const float (&v)[TN], float sl2, float nm, int lim,
+                                         uint32_t ts, float (&rp)[8]) {
 #pragma unroll
   for (int e = 0; e < 8; ++e) rp[e] = 0.f;
 #pragma unroll
@@ -135,13 +136,21 @@ __device__ __forceinline__ void exps_full(const float (&v)[TN], float sl2, float
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int c = h2 * 64 + 2 * e;
-      const float2 xx =
-          ffma2(make_float2(v[c], v[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
-      const float p0 = prefill_exp2(xx.x);
-      const float p1 = prefill_exp2(xx.y);
-      const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
-      rp[c & 7] = acc.x;
-      rp[(c + 1) & 7] = acc.y;
+      float p0, p1;
+      if (kMasked) {
+        p0 = c <= lim ? prefill_exp2(fmaf(v[c], sl2, nm)) : 0.f;
+        p1 = c + 1 <= lim ? prefill_exp2(fmaf(v[c + 1], sl2, nm)) : 0.f;
+        rp[c & 7] += p0;
+        rp[(c + 1) & 7] += p1;
+      } else {
+        const float2 xx =
+            ffma2(make_float2(v[c], v[c + 1]), make_float2(sl2, sl2), make_float2(nm, nm));
+        p0 = prefill_exp2(xx.x);
+        p1 = prefill_exp2(xx.y);
+        const float2 acc = fadd2(make_float2(rp[c & 7], rp[(c + 1) & 7]), make_float2(p0, p1));
+        rp[c & 7] = acc.x;
+        rp[(c + 1) & 7] = acc.y;
+      }
       pk[e] = __uint_as_float(pack_half2(p0, p1));
     }
     tmem_st32(ts + h2 * 32, pk);
@@ -524,14 +533,17 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
         const bool full = __all_sync(0xffffffffu, lim >= C::TN - 1);
         float rp[8];
         // After a row's first tile its running maximum m seldom grows by more than the slack,
-        // so a full tile first takes its exponents with m as it stands and no maximum pass:
-        // the terms are non-negative, so the tile's row sum bounds each of them, and a sum of
-        // at most 2^slack shows that no score passed m + slack. Only a warp in which some row's
-        // sum is larger (or not a number) takes the tile again in the plain order: maximum,
-        // rescale, exponents.
+        // so a tile first takes its exponents with m as it stands and no maximum pass: the
+        // terms are non-negative (masked keys give 0), so the tile's row sum bounds each of
+        // them, and a sum of at most 2^slack shows that no score passed m + slack. Only a warp
+        // in which some row's sum is larger (or not a number) takes the tile again in the
+        // plain order: maximum, rescale, exponents.
         bool redo = true;
-        if (full && j > 0) {
-          exps_full<C::TN>(v, sl2, -m, ts, rp);
+        if (j > 0) {
+          if (full)
+            exps_row<C::TN, false>(v, sl2, -m, lim, ts, rp);
+          else
+            exps_row<C::TN, true>(v, sl2, -m, lim, ts, rp);
           const float tsum =
               ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
           redo = __any_sync(0xffffffffu, !(tsum <= kPrefillSlackBound));
@@ -585,26 +597,10 @@ __global__ void __launch_bounds__(kPrefill2Threads, 1)
           // P = exp2(s * scale * log2e - m) as fp16 pairs over the first 64 columns of S (the
           // scale is folded into one FFMA per score; masked keys give exactly 0)
           const float nm = -m;
-          if (full) {
-            exps_full<C::TN>(v, sl2, nm, ts, rp);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) rp[e] = 0.f;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              float pk[32];
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int c = h2 * 64 + 2 * e;
-                const float p0 = c <= lim ? prefill_exp2(fmaf(v[c], sl2, nm)) : 0.f;
-                const float p1 = c + 1 <= lim ? prefill_exp2(fmaf(v[c + 1], sl2, nm)) : 0.f;
-                rp[(2 * e) & 7] += p0;
-                rp[(2 * e + 1) & 7] += p1;
-                pk[e] = __uint_as_float(pack_half2(p0, p1));
-              }
-              tmem_st32(ts + h2 * 32, pk);
-            }
-          }
+          if (full)
+            exps_row<C::TN, false>(v, sl2, nm, lim, ts, rp);
+          else
+            exps_row<C::TN, true>(v, sl2, nm, lim, ts, rp);
         }
         l += ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
         tmem_wait_st();
