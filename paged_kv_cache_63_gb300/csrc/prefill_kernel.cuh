@@ -14,9 +14,9 @@
 // CTAs that have not started (cluster launch control) and publishes their items, so a CTA
 // runs item after item with its TMEM, barriers and rings (counted across items) kept.
 // Warp roles (8 warps): 0 loads K with TMA, 6 loads Q and V; 1 owns TMEM and issues the
-// MMAs from one thread; 2..5 run the softmax, one query row per thread (TMEM lane = row),
-// rescale O in TMEM when a row's running maximum grows by more than 2^8, and write the
-// output; 7 schedules.
+// MMAs warp-collectively (one elected lane of the converged warp); 2..5 run the softmax, one
+// query row per thread (TMEM lane = row), rescale O in TMEM when a row's running maximum
+// grows by more than 2^8, and write the output; 7 schedules.
 // Every mbarrier wait is bounded; a wait that expires raises PA_DEVERR_TIMEOUT, the other
 // roles stop at their next wait, in-flight copies and MMAs are drained and TMEM is freed.
 #pragma once
