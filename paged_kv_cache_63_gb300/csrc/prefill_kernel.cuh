@@ -575,14 +575,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool full = lim >= C::TN - 1;
         float rp[8];
         // After a row's first tile its running maximum m seldom grows by more than the slack,
-        // so when no row of the warp masks a key of this tile the exponents are first taken
-        // with m as it stands and no maximum pass: the terms are non-negative, so the tile's
-        // row sum bounds each of them, and a sum of at most 2^slack shows that no score passed
-        // m + slack. Only a warp in which some row's sum is larger (or not a number) reloads
-        // the scores and takes the plain order: maximum, rescale, exponents.
+        // so a tile first takes its exponents with m as it stands and no maximum pass: the
+        // terms are non-negative (masked keys give 0), so the tile's row sum bounds each of
+        // them, and a sum of at most 2^slack shows that no score passed m + slack. Only a warp
+        // in which some row's sum is larger (or not a number) reloads the scores and takes
+        // the plain order: maximum, rescale, exponents.
         bool redo = true;
-        if (j > 0 && __all_sync(0xffffffffu, full)) {
-          exps_row<C::TN>(x, sl2, -m, true, lim, rp);
+        if (j > 0) {
+          if (__all_sync(0xffffffffu, full))
+            exps_row<C::TN>(x, sl2, -m, true, lim, rp);  // no key of the warp's rows masked
+          else
+            exps_row<C::TN>(x, sl2, -m, full, lim, rp);
           const float tsum =
               ((rp[0] + rp[1]) + (rp[2] + rp[3])) + ((rp[4] + rp[5]) + (rp[6] + rp[7]));
           redo = __any_sync(0xffffffffu, !(tsum <= kPrefillSlackBound));
