@@ -69,8 +69,12 @@ constexpr int kPrefillVWarp = 6;
 constexpr int kPrefillSchedWarp = 7;
 // warps that read each published work item: 0, 1, the softmax warps 2..5 and 6
 constexpr int kItemReaders1 = 7;
-constexpr float kPrefillRescaleSlack = 8.f;  // log2 units: O is rescaled when m grows > 2^8
-constexpr float kPrefillSlackBound = 256.f;  // 2^kPrefillRescaleSlack
+// O is rescaled only when a row's running maximum grows by more than 2^kPrefillSlackLog2;
+// until then every exponent term is at most kPrefillSlackBound, which a tile's row sum may
+// therefore be checked against.
+constexpr int kPrefillSlackLog2 = 8;
+constexpr float kPrefillRescaleSlack = static_cast<float>(kPrefillSlackLog2);  // log2 units
+constexpr float kPrefillSlackBound = static_cast<float>(1 << kPrefillSlackLog2);
 
 // Barrier slots.
 enum : int {
